@@ -1,0 +1,230 @@
+"""fp64 CPU oracle for weight-absorbed MLA decode -- TEST INFRASTRUCTURE.
+
+This package is the checker, not the product.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import it.  It shares no code with the CUDA library and never
+imports it; the two meet only through the seeded input generators, which hold
+none of the method's arithmetic.
+
+The numerics live in ``mla_oracle.c`` (plain fp64 loops, OpenMP over output
+rows), compiled on first use with the host C compiler; ``counts.py`` holds the
+closed-form FLOP / byte counters the pages print.  Inputs are the exact bf16
+tensors handed to the GPU (bit patterns, widened to fp64 inside the C code);
+activations returned here are float64 CPU tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``mla_oracle.c`` into ``liboracle.so`` (skipped when up to date)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True,
+                       stdout=subprocess.PIPE, stderr=subprocess.PIPE)
+    except subprocess.CalledProcessError:
+        # No OpenMP runtime on this host: the pragmas are ignored, results are identical.
+        subprocess.run(base, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("s_q", ctypes.c_int),
+                ("d_c", ctypes.c_int), ("d_rope", ctypes.c_int), ("d_nope", ctypes.c_int),
+                ("d_v", ctypes.c_int), ("scale", ctypes.c_double)]
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("kv", ctypes.c_void_p), ("seq_stride", ctypes.c_longlong),
+                ("block_table", ctypes.c_void_p), ("max_pages", ctypes.c_int),
+                ("page_size", ctypes.c_int), ("capacity", ctypes.c_longlong),
+                ("seq_lens", ctypes.c_void_p)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, LL = ctypes.c_void_p, ctypes.c_longlong
+            lib.orc_threads.restype = ctypes.c_int
+            lib.orc_absorb_q.argtypes = [ctypes.POINTER(_Dims), P, P, P, P]
+            lib.orc_attend.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache), P, LL, P, P]
+            lib.orc_attend_partial.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache),
+                                               LL, LL, LL, P, P, P]
+            lib.orc_combine.argtypes = [ctypes.c_int, ctypes.c_int, P, P, P, P, P]
+            lib.orc_out_proj.argtypes = [ctypes.POINTER(_Dims), P, P, P]
+            lib.orc_naive.argtypes = [ctypes.POINTER(_Dims), P, P, ctypes.POINTER(_Cache), P, P,
+                                      P, LL, P, P]
+            _lib = lib
+    return _lib
+
+
+def threads() -> int:
+    """OpenMP threads the oracle uses (the host's affinity unless OMP_NUM_THREADS says otherwise)."""
+    return int(_load().orc_threads())
+
+
+# ----------------------------------------------------------------------------- marshalling
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    """bf16 tensor -> contiguous int16 view of its bit patterns (CPU)."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"oracle expects bf16 inputs, got {t.dtype}")
+    return t.detach().to("cpu").contiguous().view(torch.int16)
+
+
+def _f64(t: torch.Tensor) -> torch.Tensor:
+    return t.detach().to("cpu", torch.float64).contiguous()
+
+
+def _i32(t: torch.Tensor) -> torch.Tensor:
+    return t.detach().to("cpu", torch.int32).contiguous()
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dims(d) -> _Dims:
+    return _Dims(int(d.B), int(d.H), int(d.s_q), int(d.d_c), int(d.d_rope), int(d.d_nope),
+                 int(d.d_v), float(d.scale))
+
+
+class _CacheArgs:
+    """Keeps the marshalled cache tensors alive while the C call runs.
+
+    Contiguous cache: ``kv`` is [B, T_max, d_c + d_rope] (any strides; copied
+    contiguous here).  Paged cache: ``kv`` is the pool [P, page_size, d_c + d_rope]
+    and ``block_table`` is [B, max_pages]."""
+
+    def __init__(self, d, kv, seq_lens, block_table=None, page_size=64):
+        self.kv = _bits(kv)
+        self.seq_lens = _i32(seq_lens)
+        self.block_table = _i32(block_table) if block_table is not None else None
+        W = d.d_c + d.d_rope
+        if int(kv.shape[-1]) != W:
+            raise ValueError("cache rows must be d_c + d_rope wide")
+        if self.block_table is None:
+            t_max = int(kv.shape[1])
+            self.c = _Cache(_ptr(self.kv).value, t_max * W, None, 0, int(page_size), t_max,
+                            _ptr(self.seq_lens).value)
+        else:
+            max_pages = int(self.block_table.shape[1])
+            self.c = _Cache(_ptr(self.kv).value, 0, _ptr(self.block_table).value, max_pages,
+                            int(page_size), max_pages * int(page_size), _ptr(self.seq_lens).value)
+
+
+def _rows_arg(rows):
+    if rows is None:
+        return None, 0
+    r = torch.as_tensor(np.asarray(rows, dtype=np.int64)).contiguous()
+    return r, int(r.numel())
+
+
+# ----------------------------------------------------------------------------- public API
+def absorb_q(d, q_nope, q_rope, w_uk) -> torch.Tensor:
+    """q_cat [B, s_q, H, d_c + d_rope] float64 (see orc_absorb_q)."""
+    lib = _load()
+    qn, qr, wk = _bits(q_nope), _bits(q_rope), _bits(w_uk)
+    out = torch.empty(d.B, d.s_q, d.H, d.d_c + d.d_rope, dtype=torch.float64)
+    lib.orc_absorb_q(ctypes.byref(_dims(d)), _ptr(qn), _ptr(qr), _ptr(wk), _ptr(out))
+    return out
+
+
+def attend(d, q_cat, kv, seq_lens, block_table=None, page_size=64, rows=None):
+    """(o_lat [B, s_q, H, d_c], lse [B, s_q, H]) float64 from a float64-widened q_cat.
+
+    ``rows`` optionally lists flat row indices (b*s_q + i)*H + h to compute; other
+    rows are returned as NaN."""
+    lib = _load()
+    q = _f64(q_cat)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    o = torch.full((d.B, d.s_q, d.H, d.d_c), float("nan"), dtype=torch.float64)
+    lse = torch.full((d.B, d.s_q, d.H), float("nan"), dtype=torch.float64)
+    r, n = _rows_arg(rows)
+    lib.orc_attend(ctypes.byref(_dims(d)), _ptr(q), ctypes.byref(ca.c), _ptr(r), n, _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attend_partial(d, q_cat, kv, seq_lens, row, j0, j1, block_table=None, page_size=64):
+    """Unnormalised partial (m, l, acc[d_c]) of one flat row over tokens [j0, j1)."""
+    lib = _load()
+    q = _f64(q_cat)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    m = torch.zeros(1, dtype=torch.float64)
+    l = torch.zeros(1, dtype=torch.float64)
+    acc = torch.zeros(d.d_c, dtype=torch.float64)
+    lib.orc_attend_partial(ctypes.byref(_dims(d)), _ptr(q), ctypes.byref(ca.c), int(row), int(j0),
+                           int(j1), _ptr(m), _ptr(l), _ptr(acc))
+    return float(m.item()), float(l.item()), acc
+
+
+def combine(m, l, acc):
+    """Merge partials: m, l [n] and acc [n, width] -> (o [width], lse)."""
+    lib = _load()
+    m = _f64(torch.as_tensor(m, dtype=torch.float64))
+    l = _f64(torch.as_tensor(l, dtype=torch.float64))
+    acc = _f64(torch.as_tensor(acc, dtype=torch.float64))
+    n, width = int(acc.shape[0]), int(acc.shape[1])
+    o = torch.zeros(width, dtype=torch.float64)
+    lse = torch.zeros(1, dtype=torch.float64)
+    lib.orc_combine(n, width, _ptr(m), _ptr(l), _ptr(acc), _ptr(o), _ptr(lse))
+    return o, float(lse.item())
+
+
+def out_proj(d, o_lat, w_uv) -> torch.Tensor:
+    """out [B, s_q, H, d_v] float64 from a float64-widened o_lat."""
+    lib = _load()
+    o = _f64(o_lat)
+    wv = _bits(w_uv)
+    out = torch.empty(d.B, d.s_q, d.H, d.d_v, dtype=torch.float64)
+    lib.orc_out_proj(ctypes.byref(_dims(d)), _ptr(o), _ptr(wv), _ptr(out))
+    return out
+
+
+def naive(d, q_nope, q_rope, kv, seq_lens, w_uk, w_uv, block_table=None, page_size=64, rows=None):
+    """Naive decompress-then-attend: (out [B, s_q, H, d_v], lse [B, s_q, H]) float64."""
+    lib = _load()
+    qn, qr, wk, wv = _bits(q_nope), _bits(q_rope), _bits(w_uk), _bits(w_uv)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    out = torch.full((d.B, d.s_q, d.H, d.d_v), float("nan"), dtype=torch.float64)
+    lse = torch.full((d.B, d.s_q, d.H), float("nan"), dtype=torch.float64)
+    r, n = _rows_arg(rows)
+    lib.orc_naive(ctypes.byref(_dims(d)), _ptr(qn), _ptr(qr), ctypes.byref(ca.c), _ptr(wk), _ptr(wv),
+                  _ptr(r), n, _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def decode(d, q_nope, q_rope, kv, seq_lens, w_uk, w_uv, block_table=None, page_size=64, rows=None):
+    """Absorbed decode end to end in fp64: dict(q_cat, o_lat, lse, out).
+
+    With ``rows`` the attention runs on those rows only; out is then valid on
+    those rows only."""
+    q_cat = absorb_q(d, q_nope, q_rope, w_uk)
+    o_lat, lse = attend(d, q_cat, kv, seq_lens, block_table, page_size, rows)
+    out = out_proj(d, torch.nan_to_num(o_lat, nan=0.0) if rows is not None else o_lat, w_uv)
+    if rows is not None:
+        keep = torch.zeros(d.B * d.s_q * d.H, dtype=torch.bool)
+        keep[torch.as_tensor(np.asarray(rows, dtype=np.int64))] = True
+        out.view(-1, d.d_v)[~keep] = float("nan")
+    return {"q_cat": q_cat, "o_lat": o_lat, "lse": lse, "out": out}
