@@ -1,0 +1,460 @@
+#!/usr/bin/env python3
+"""Benchmark of one absorbed-MLA decode step (absorb_q -> decode_attn -> out_proj).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config dsv3] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0.  A step is one pass of the whole hot path over
+one batch of synthetic inputs already resident in HBM.  Under torchrun each rank
+runs an independent replica on its own GPU (sequences never read each other's
+cache, so the batch shards with no data-path collective: weak scaling); the
+step time is the maximum over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the slow baseline arm)."""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mla_decode_attention_absorbed_gb300.workloads import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "MLA decode TFLOP/s, HBM TB/s & roofline fraction (H=128, d_c=512+64, 1×GB300)"
+DEFAULT_CONFIG = "dsv3"
+L2_BYTES = 129 * 2 ** 20
+
+
+# ------------------------------------------------------------------------- distributed plumbing
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return False
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return True
+
+
+def barrier(active: bool):
+    if active:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(x: float, active: bool, device="cpu") -> float:
+    """Maximum of a host scalar over ranks (timing only: no data-path collective)."""
+    if not active:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(cfg_seed: int, rank: int) -> int:
+    """Each rank decodes its own independent batch."""
+    return cfg_seed + 1000 * rank
+
+
+# ------------------------------------------------------------------------- algorithmic work
+def work(cfg, seq_lens):
+    from oracle import counts  # closed-form counters, pinned against the pages
+    lens = [int(x) for x in seq_lens]
+    B, H, s_q = cfg.B, cfg.H, cfg.s_q
+    attn_f = counts.attention_flops(H, cfg.d_c, cfg.d_rope, lens, s_q)
+    attn_b = counts.attention_bytes(H, cfg.d_c, cfg.d_rope, lens, s_q)
+    abs_f = counts.absorb_flops(B, s_q, H, cfg.d_nope, cfg.d_c)
+    abs_b = counts.absorb_bytes(B, s_q, H, cfg.d_nope, cfg.d_c, cfg.d_rope)
+    out_f = counts.out_proj_flops(B, s_q, H, cfg.d_c, cfg.d_v)
+    out_b = counts.out_proj_bytes(B, s_q, H, cfg.d_c, cfg.d_v)
+    pairs = sum(counts.visible_pairs(L, s_q) for L in lens)
+    return dict(attn_flops=attn_f, attn_bytes=attn_b, step_flops=attn_f + abs_f + out_f,
+                step_bytes=attn_b + abs_b + out_b, pairs=pairs, tokens=B * s_q,
+                cache_bytes=sum(lens) * (cfg.d_c + cfg.d_rope) * 2)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def traffic_for(kernel_key: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current source of that kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d:
+        return None
+    if d.get("source_sha256") != source_hash():
+        return None
+    return d.get("bytes_per_launch")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_decode_attention_absorbed_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# ------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------- our arm
+def run_ours(cfg, args, rank, world, local, active):
+    from mla_decode_attention_absorbed_gb300 import mla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mla.load()
+    c = cfg.with_(seed=replica_seed(cfg.seed, rank))
+    inp = make_inputs(c)
+    w = work(c, inp["seq_lens"].tolist())
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    prob = mla.Problem.of(c)
+    dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], c.page_size,
+                      max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits)
+    splits = mla.decode_num_splits(prob, dec.cache) if args.splits == 0 else args.splits
+    q_nope, q_rope = d["q_nope"], d["q_rope"]
+    stream = torch.cuda.current_stream(dev)
+
+    flush = None
+    if w["cache_bytes"] < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        dec(q_nope, q_rope)
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st = mla.read_status(dec.workspace)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier(active)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for k in range(K):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        dec.absorb(q_nope, q_rope)
+        ev_attn[k][0].record(stream)
+        dec.attend()
+        ev_attn[k][1].record(stream)
+        dec.project()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(active)
+    t_wall = time.perf_counter() - t_wall
+    clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
+    ms_local = sum(step_ms) / K
+    ms = reduce_max(ms_local, active, "cuda" if active and args.backend == "nccl" else "cpu")
+    attn_avg = sum(attn_ms) / K
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    h_qn = inp["q_nope"].pin_memory()
+    h_qr = inp["q_rope"].pin_memory()
+    h_lens = inp["seq_lens"].pin_memory()
+    h_bt = inp["block_table"].pin_memory() if inp["block_table"] is not None else None
+    h_out = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    e2e_steps = max(3, min(K, 50))
+    h2d = h_qn.numel() * 2 + h_qr.numel() * 2 + h_lens.numel() * 4 + (h_bt.numel() * 4 if h_bt is not None else 0)
+    d2h = h_out.numel() * 2
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(active)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        q_nope.copy_(h_qn, non_blocking=True)
+        q_rope.copy_(h_qr, non_blocking=True)
+        d["seq_lens"].copy_(h_lens, non_blocking=True)
+        if h_bt is not None:
+            d["block_table"].copy_(h_bt, non_blocking=True)
+        step()
+        h_out.copy_(dec.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active,
+                        "cuda" if active and args.backend == "nccl" else "cpu")
+
+    # parity spot check of the timed configuration (a few rows against the oracle)
+    return dict(w=w, ms=ms, attn_ms=attn_avg, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h, splits=splits, clocks=clocks,
+                step_ms=step_ms, wall_s=t_wall, inp=inp, c=c, launches_per_step=3 + (1 if splits > 1 else 0))
+
+
+def cpu_baseline(cfg, inp, budget_s: float = 12.0):
+    """The oracle as it stands, absorbed form, on whole sequences of the same
+    workload until about ``budget_s`` of host time is spent."""
+    import oracle
+    from oracle import counts
+    threads = oracle.threads()
+    B = cfg.B
+    done_flops, t_used, n = 0, 0.0, 0
+    for b in range(B):
+        sub = cfg.with_(B=1)
+        one = {k: inp[k][b:b + 1] for k in ("q_nope", "q_rope", "seq_lens")}
+        if inp["block_table"] is None:
+            kv = inp["kv"][b:b + 1]
+            bt = None
+        else:
+            kv, bt = inp["kv"], inp["block_table"][b:b + 1]
+        t0 = time.perf_counter()
+        oracle.decode(sub, one["q_nope"], one["q_rope"], kv, one["seq_lens"], inp["w_uk"], inp["w_uv"],
+                      block_table=bt, page_size=cfg.page_size)
+        t_used += time.perf_counter() - t0
+        L = int(one["seq_lens"][0])
+        done_flops += (counts.attention_flops(cfg.H, cfg.d_c, cfg.d_rope, [L], cfg.s_q)
+                       + counts.absorb_flops(1, cfg.s_q, cfg.H, cfg.d_nope, cfg.d_c)
+                       + counts.out_proj_flops(1, cfg.s_q, cfg.H, cfg.d_c, cfg.d_v))
+        n += 1
+        if t_used >= budget_s:
+            break
+    return {"value": done_flops / t_used / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {B} sequences of the {cfg.name} workload, whole absorbed step (fp64), "
+                      f"{t_used:.1f} s"}
+
+
+def workload_name(cfg):
+    lens = f"T={cfg.T}" if not cfg.len_lo else f"L~U[{cfg.len_lo},{cfg.len_hi}]"
+    lay = f"paged{cfg.page_size}" if cfg.paged else "contiguous"
+    return (f"{cfg.name}: B={cfg.B} H={cfg.H} d_c={cfg.d_c} d_rope={cfg.d_rope} d_nope={cfg.d_nope} "
+            f"d_v={cfg.d_v} {lens} s_q={cfg.s_q} {lay} bf16")
+
+
+def main_ours(args):
+    rank, world, local = dist_env()
+    active = init_dist(world, args.backend)
+    cfg = CONFIGS[args.config]
+    r = run_ours(cfg, args, rank, world, local, active)
+    if rank != 0:
+        return
+    w, ms = r["w"], r["ms"]
+    pk = peaks()
+    total_flops = w["step_flops"] * world
+    value = total_flops / (ms * 1e-3) / 1e12
+    tensor_bound = w["attn_flops"] / (pk["bf16_tflops"] * 1e12) > w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)
+    attn_s = r["attn_ms"] * 1e-3
+    if tensor_bound:
+        achieved = w["attn_flops"] / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"]}
+    else:
+        achieved = w["attn_bytes"] / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"]}
+    roof["traffic"] = traffic_for(f"attn:{cfg.name}")
+    roof["kernel"] = "mla_decode_attn (split-T attention + LSE combine)"
+    roof["peak_source"] = pk["source"] + (" burst bf16" if tensor_bound else " HBM copy")
+    roof["roofline_time_us"] = max(w["attn_flops"] / (pk["bf16_tflops"] * 1e12),
+                                   w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)) * 1e6
+    roof["kernel_us"] = r["attn_ms"] * 1e3
+    cpu = cpu_baseline(r["c"], r["inp"], args.cpu_budget) if not args.no_cpu_baseline else None
+    clk = r["clocks"].summary()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights)",
+        "config": {"workload": workload_name(cfg), "num_splits": r["splits"],
+                   "l2": ("inputs larger than L2: the cache alone is "
+                          f"{w['cache_bytes'] / 1e6:.0f} MB per replica") if w["cache_bytes"] >= 2 * L2_BYTES
+                   else "L2 flushed between steps (256 MB write)",
+                   "parallelism": f"{world} independent replica(s), sequences sharded by rank"},
+        "hbm_tbps": (w["step_bytes"] * world) / (ms * 1e-3) / 1e12,
+        "attn_tflops": w["attn_flops"] / attn_s / 1e12,
+        "attn_tbps": w["attn_bytes"] / attn_s / 1e12,
+        "attended_tokens_per_s": w["pairs"] * world / (ms * 1e-3),
+        "decode_tokens_per_s": w["tokens"] * world / (ms * 1e-3),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": total_flops / (r["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": r["e2e_ms"], "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
+                "note": "pinned host q_nope/q_rope/seq_lens(/block_table) in, out back, every step; "
+                        "latent cache and weights stay resident in HBM"},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+        "clocks": clk,
+        "step_ms_min": min(r["step_ms"]),
+        "step_ms_median": statistics.median(r["step_ms"]),
+    }
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------------- reference arm
+def main_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from oracle import counts
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg)
+    threads = oracle.threads()
+    # each step: the whole absorbed step for one sequence of the workload (bounded sample)
+    def one(b):
+        sub = cfg.with_(B=1)
+        kv = inp["kv"][b:b + 1] if inp["block_table"] is None else inp["kv"]
+        bt = None if inp["block_table"] is None else inp["block_table"][b:b + 1]
+        oracle.decode(sub, inp["q_nope"][b:b + 1], inp["q_rope"][b:b + 1], kv, inp["seq_lens"][b:b + 1],
+                      inp["w_uk"], inp["w_uv"], block_table=bt, page_size=cfg.page_size)
+        L = int(inp["seq_lens"][b])
+        return (counts.attention_flops(cfg.H, cfg.d_c, cfg.d_rope, [L], cfg.s_q)
+                + counts.absorb_flops(1, cfg.s_q, cfg.H, cfg.d_nope, cfg.d_c)
+                + counts.out_proj_flops(1, cfg.s_q, cfg.H, cfg.d_c, cfg.d_v))
+
+    for k in range(args.warmup):
+        one(k % cfg.B)
+    flops, t = 0, 0.0
+    times = []
+    for k in range(args.steps):
+        t0 = time.perf_counter()
+        flops += one(k % cfg.B)
+        dt = time.perf_counter() - t0
+        times.append(dt)
+        t += dt
+    value = flops / t / 1e12
+    ms = t / args.steps * 1e3
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": workload_name(cfg),
+                   "sample": "each step = the whole absorbed decode of one sequence (all heads) of this workload"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} sequence(s) of {cfg.B}, one per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def parse(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--splits", type=int, default=0, help="split count (0 = the library's choice)")
+    ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args(argv)
+    if a.warmup < 3:
+        a.warmup = 3
+    if a.steps is None:
+        a.steps = 2 if a.impl == "reference" else 200
+    return a
+
+
+if __name__ == "__main__":
+    args = parse()
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)

@@ -1,0 +1,177 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) weight-absorbed MLA decode library.
+ *
+ * One decode step of one attention layer, with the key up-projection folded
+ * into the query and the value up-projection applied after the latent-space sum
+ * ("MLA, dim by dim", section "MLA Decode": decode score order and decode value
+ * order; "Why MLA and MTP Fight Each Other: Attention Through Arithmetic
+ * Intensity", sections 3.1-3.3 and Appendix A):
+ *
+ *   mla_absorb_q     q_cat = [ q_nope . W_UK^T | q_rope ]          per head
+ *   mla_decode_attn  o_lat, lse = softmax(scale * q_cat . [c_kv|k_rope]^T) . c_kv
+ *                    over a contiguous or paged latent cache, split along the
+ *                    history and merged with a log-sum-exp combine
+ *   mla_out_proj     out = o_lat . W_UV                               per head
+ *   mla_naive_decode the decompress-then-attend form, a comparison point only
+ *                    ("The MLA decode speedup hiding in your model card",
+ *                    section "The naive form, written out")
+ *
+ * Conventions for every entry point:
+ *  - Pointers named for tensors are DEVICE pointers owned by the caller; the
+ *    library never allocates, frees or keeps them.  Scratch memory is the
+ *    caller's `workspace`, sized by the matching *_workspace_size query.
+ *  - Tensors are dense row-major in the layouts stated, bf16 unless stated.
+ *    Every tensor base pointer and the workspace must be 16-byte aligned.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise, except mla_read_status.
+ *  - Every argument is checked on the host before anything is launched.  A
+ *    non-zero return means nothing was launched, except MLA_ERR_CUDA, which
+ *    reports a failed launch.  Problems only the device can see (a sequence
+ *    length or block-table entry out of range, a bounded wait that ran out) are
+ *    written to the status word at the start of the workspace; read it with
+ *    mla_read_status.  The affected sequence's outputs are written as zeros
+ *    (lse = -inf); nothing faults and nothing reads outside the caller's buffers.
+ *  - Dimensions: H >= 1, s_q >= 1, d_c a multiple of 64 up to 512, d_rope a
+ *    multiple of 16 up to 64, d_nope and d_v multiples of 16 from 16 to 256,
+ *    s_q * H <= 4096.  Other shapes return MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_H
+#define MLA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_NULL = 1,        /* a required pointer is NULL */
+    MLA_ERR_SHAPE = 2,       /* a size is negative or sizes disagree */
+    MLA_ERR_SEQLEN = 3,      /* device: seq_lens[b] outside [s_q, capacity] */
+    MLA_ERR_ALIGN = 4,       /* a pointer or stride is not 16-byte aligned */
+    MLA_ERR_WORKSPACE = 5,   /* workspace smaller than the size query returned */
+    MLA_ERR_UNSUPPORTED = 6, /* shape outside the supported envelope above */
+    MLA_ERR_CUDA = 7,        /* a CUDA runtime call or launch failed */
+    MLA_ERR_TIMEOUT = 8,     /* device: a bounded wait gave up (no hang, no fault) */
+    MLA_ERR_PAGE = 9         /* device: a block-table entry outside [0, num_pages) */
+} mla_status;
+
+/* Problem sizes ("MLA, dim by dim", Notation and Preliminaries; the decoupled
+ * RoPE width is Appendix A's d_s).  scale multiplies every score; callers use
+ * 1/sqrt(d_nope + d_rope). */
+typedef struct {
+    int B;        /* sequences in the batch */
+    int H;        /* query heads */
+    int s_q;      /* new query tokens per sequence (1 = decode, >1 = verify) */
+    int d_c;      /* latent width (c_kv), 512 for DeepSeek-V3 */
+    int d_rope;   /* decoupled RoPE key width, 64 for DeepSeek-V3 */
+    int d_nope;   /* per-head no-RoPE query/key width absorbed through W_UK */
+    int d_v;      /* per-head value width produced by W_UV */
+    float scale;  /* softmax scale */
+} mla_dims;
+
+/* The latent cache: one row [c_kv (d_c) | k_rope (d_rope)] per cached token,
+ * shared by every head ("Decode attention intensity is fixed at the
+ * query-to-KV head ratio...", "A strong answer": 512 + 64 = 576 values, 1,152 B
+ * in bf16).  seq_lens[b] counts the s_q new tokens, which are already
+ * appended; query i (0-based) of sequence b sees tokens j <= seq_lens[b] - s_q + i. */
+typedef struct {
+    const void *kv;          /* bf16. block_table == NULL: contiguous, sequence b's
+                                token j at kv + b*seq_stride + j*(d_c+d_rope).
+                                Otherwise the pool [num_pages][page_size][d_c+d_rope]. */
+    long long seq_stride;    /* contiguous: elements between sequences, a multiple of 8,
+                                >= capacity*(d_c+d_rope) */
+    int capacity;            /* contiguous: tokens each sequence may hold */
+    const int *block_table;  /* NULL => contiguous; else device int32 [B][max_pages]:
+                                token j of sequence b lives in pool page
+                                block_table[b*max_pages + j/page_size], row j%page_size */
+    int max_pages;           /* paged: columns of block_table */
+    int page_size;           /* paged: tokens per page, a multiple of 64 */
+    int num_pages;           /* paged: pages in the pool (entries are checked against it) */
+    const int *seq_lens;     /* device int32 [B] */
+    int max_seq_len;         /* host upper bound of seq_lens used to plan the split;
+                                0 means capacity (contiguous) or max_pages*page_size */
+} mla_cache;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+MLA_API const char *mla_status_string(int status);
+
+/* ABI version of this header: bumps when a signature or struct changes. */
+MLA_API int mla_abi_version(void);
+
+/* Absorb W_UK into the query and append the RoPE query ("MLA, dim by dim",
+ * "MLA Decode", decode score order; "Why MLA and MTP Fight Each Other", 3.1):
+ *   q_cat[b,i,h, 0:d_c]          = sum_n q_nope[b,i,h,n] * W_UK[h,c,n]  (fp32 accumulate)
+ *   q_cat[b,i,h, d_c:d_c+d_rope] = q_rope[b,i,h,:]
+ * q_nope [B][s_q][H][d_nope], q_rope [B][s_q][H][d_rope], w_uk [H][d_c][d_nope],
+ * q_cat [B][s_q][H][d_c+d_rope]; all bf16, outputs rounded to nearest even. */
+MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q_rope,
+                         const void *w_uk, void *q_cat, void *stream);
+
+/* Bytes of workspace mla_decode_attn needs for this problem and split count
+ * (num_splits 0 = the library's choice).  Returns 0 for invalid arguments. */
+MLA_API size_t mla_decode_workspace_size(const mla_dims *dims, const mla_cache *cache,
+                                         int num_splits);
+
+/* Split count mla_decode_attn uses for num_splits == 0 (a function of the dims,
+ * B and the max_seq_len hint only).  Returns 0 for invalid arguments. */
+MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
+
+/* Latent-space attention of every head against the shared latent cache
+ * ("MLA, dim by dim", "Why RoPE Gets in the Way", decoupled score, and "MLA
+ * Decode", fused decode kernel; "Why MLA and MTP Fight Each Other", 3.2 and
+ * section 4's fused streaming condition: each latent tile is read once and
+ * serves both the score and the weighted sum):
+ *   s_j   = scale * q_cat[b,i,h,:] . kv_row_j                (all d_c+d_rope columns)
+ *   lse   = log sum_j exp(s_j)          over visible j      (natural log, fp32)
+ *   o_lat = sum_j exp(s_j - lse) * kv_row_j[0:d_c]           (bf16, fp32 accumulate)
+ * The history of each sequence is cut into num_splits pieces processed in
+ * parallel, each keeping an online softmax; the pieces are merged with a
+ * log-sum-exp combine.  q_cat [B][s_q][H][d_c+d_rope]; o_lat [B][s_q][H][d_c];
+ * lse fp32 [B][s_q][H].  num_splits 0 = the library's choice, else 1..64. */
+MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
+                            void *o_lat, float *lse, void *workspace, size_t ws_bytes,
+                            int num_splits, void *stream);
+
+/* Project the latent-space output to each head's value width ("MLA, dim by dim",
+ * "MLA Decode", decode value order; "Why MLA and MTP Fight Each Other", 3.2):
+ *   out[b,i,h,v] = sum_c o_lat[b,i,h,c] * W_UV[h,c,v]   (fp32 accumulate, bf16 out)
+ * o_lat [B][s_q][H][d_c], w_uv [H][d_c][d_v], out [B][s_q][H][d_v]. */
+MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_uv,
+                         void *out, void *stream);
+
+/* Bytes of workspace mla_naive_decode needs: the materialised per-head K and V
+ * of every visible cached token (B*H*capacity*(d_nope+d_v) bf16) plus the
+ * status word.  Returns 0 for invalid arguments. */
+MLA_API size_t mla_naive_workspace_size(const mla_dims *dims, const mla_cache *cache);
+
+/* Decompress-then-attend, the comparison path ("The MLA decode speedup hiding
+ * in your model card", "The naive form, written out"; "Decode attention
+ * intensity...", the 33.6 MFLOP per cached token decompression): for every head
+ * and every cached token, K = c_kv . W_UK[h] and V = c_kv . W_UV[h] are written
+ * to the workspace, then standard attention runs with the RoPE key appended:
+ *   s_j = scale * (q_nope . K_j + q_rope . k_rope_j),  out = sum_j softmax(s)_j V_j.
+ * Same tensors as the absorbed path; out [B][s_q][H][d_v] bf16, lse fp32 [B][s_q][H]. */
+MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const void *q_rope,
+                             const mla_cache *cache, const void *w_uk, const void *w_uv,
+                             void *out, float *lse, void *workspace, size_t ws_bytes,
+                             void *stream);
+
+/* Wait for `stream`, then copy the device status word at the start of
+ * `workspace` (written by the last mla_decode_attn / mla_naive_decode that used
+ * it) into *status: MLA_OK, MLA_ERR_SEQLEN, MLA_ERR_PAGE or MLA_ERR_TIMEOUT.
+ * Returns MLA_ERR_CUDA if the copy or the wait fails. */
+MLA_API int mla_read_status(const void *workspace, int *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H */

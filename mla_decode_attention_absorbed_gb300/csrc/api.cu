@@ -1,0 +1,225 @@
+// C ABI of the MLA decode library: argument checks, workspace layout, launches.
+// Declarations and the contract live in include/mla.h.
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr int kMaxSplits = 64;
+constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (split planning only)
+constexpr size_t kStatusBytes = 256;  // status word + padding at the workspace start
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int check_dims(const mla_dims *d) {
+    if (!d) return MLA_ERR_NULL;
+    if (d->B < 0 || d->H < 1 || d->s_q < 1 || d->d_c < 1 || d->d_rope < 0 || d->d_nope < 1 || d->d_v < 1)
+        return MLA_ERR_SHAPE;
+    if (d->d_c % 64 || d->d_c > 512) return MLA_ERR_UNSUPPORTED;
+    if (d->d_rope % 16 || d->d_rope > 64) return MLA_ERR_UNSUPPORTED;
+    if (d->d_nope % 16 || d->d_nope > 256) return MLA_ERR_UNSUPPORTED;
+    if (d->d_v % 16 || d->d_v > 256) return MLA_ERR_UNSUPPORTED;
+    if ((long long)d->s_q * d->H > 4096) return MLA_ERR_UNSUPPORTED;
+    if (!(d->scale == d->scale)) return MLA_ERR_SHAPE;  // NaN scale
+    return MLA_OK;
+}
+
+// Capacity (tokens per sequence) of a checked cache.
+long long cache_capacity(const mla_cache *c) {
+    return c->block_table ? (long long)c->max_pages * c->page_size : (long long)c->capacity;
+}
+
+int check_cache(const mla_dims *d, const mla_cache *c) {
+    if (!c) return MLA_ERR_NULL;
+    if (d->B == 0) return MLA_OK;
+    if (!c->kv || !c->seq_lens) return MLA_ERR_NULL;
+    if (!aligned16(c->kv) || ((uintptr_t)c->seq_lens & 3u)) return MLA_ERR_ALIGN;
+    const long long W = d->d_c + d->d_rope;
+    if (c->block_table) {
+        if ((uintptr_t)c->block_table & 3u) return MLA_ERR_ALIGN;
+        if (c->max_pages < 1 || c->page_size < 1 || c->num_pages < 1) return MLA_ERR_SHAPE;
+        if (c->page_size % 64) return MLA_ERR_UNSUPPORTED;
+    } else {
+        if (c->capacity < 1) return MLA_ERR_SHAPE;
+        if (c->seq_stride < (long long)c->capacity * W) return MLA_ERR_SHAPE;
+        if (c->seq_stride % 8) return MLA_ERR_ALIGN;
+    }
+    if (c->max_seq_len < 0 || c->max_seq_len > cache_capacity(c)) return MLA_ERR_SHAPE;
+    if (cache_capacity(c) > (1ll << 30)) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
+    if (requested > 0) return requested;
+    long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
+    long long tiles = (maxL + 63) / 64;
+    long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
+    long long units = (long long)d->B * row_blocks;
+    if (units <= 0) return 1;
+    // Enough pieces to cover every SM pair once, each piece at least 8 tiles long.
+    long long want = (kNumSMs / 2 + units - 1) / units;
+    long long cap = tiles / 8;
+    if (want > cap) want = cap;
+    if (want < 1) want = 1;
+    if (want > kMaxSplits) want = kMaxSplits;
+    return (int)want;
+}
+
+size_t attn_workspace_bytes(const mla_dims *d, int splits) {
+    if (splits <= 1) return kStatusBytes;
+    size_t rows = (size_t)d->B * splits * d->s_q * d->H;
+    return kStatusBytes + round_up(rows * 2 * sizeof(float), 256) + rows * (size_t)d->d_c * sizeof(float);
+}
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+mla::AttnParams make_params(const mla_dims *d, const mla_cache *c) {
+    mla::AttnParams p;
+    memset(&p, 0, sizeof p);
+    p.B = d->B; p.H = d->H; p.s_q = d->s_q; p.d_c = d->d_c; p.d_rope = d->d_rope; p.scale = d->scale;
+    p.kv = (const __nv_bfloat16 *)c->kv;
+    p.seq_stride = c->seq_stride;
+    p.capacity = (int)cache_capacity(c);
+    p.block_table = c->block_table;
+    p.max_pages = c->max_pages; p.page_size = c->page_size; p.num_pages = c->num_pages;
+    p.seq_lens = c->seq_lens;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+MLA_API const char *mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "MLA_OK";
+        case MLA_ERR_NULL: return "MLA_ERR_NULL: a required pointer is NULL";
+        case MLA_ERR_SHAPE: return "MLA_ERR_SHAPE: a size is negative or sizes disagree";
+        case MLA_ERR_SEQLEN: return "MLA_ERR_SEQLEN: a sequence length is outside [s_q, capacity]";
+        case MLA_ERR_ALIGN: return "MLA_ERR_ALIGN: a pointer or stride is not 16-byte aligned";
+        case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace too small";
+        case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape outside the supported envelope";
+        case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA call failed";
+        case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded device wait gave up";
+        case MLA_ERR_PAGE: return "MLA_ERR_PAGE: a block-table entry is outside the pool";
+        default: return "unknown mla status";
+    }
+}
+
+MLA_API int mla_abi_version(void) { return kAbiVersion; }
+
+MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q_rope, const void *w_uk,
+                         void *q_cat, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    if (dims->B == 0) return MLA_OK;
+    if (!q_nope || !w_uk || !q_cat || (dims->d_rope && !q_rope)) return MLA_ERR_NULL;
+    if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_cat) || (q_rope && !aligned16(q_rope)))
+        return MLA_ERR_ALIGN;
+    cudaError_t e = mla::launch_absorb_q_simple(*dims, q_nope, q_rope, w_uk, q_cat, as_stream(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache) {
+    if (check_dims(dims) || check_cache(dims, cache)) return 0;
+    return plan_splits(dims, cache, 0);
+}
+
+MLA_API size_t mla_decode_workspace_size(const mla_dims *dims, const mla_cache *cache, int num_splits) {
+    if (check_dims(dims) || check_cache(dims, cache)) return 0;
+    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+    return attn_workspace_bytes(dims, plan_splits(dims, cache, num_splits));
+}
+
+MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_cache *cache, void *o_lat,
+                            float *lse, void *workspace, size_t ws_bytes, int num_splits, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    if (!cache) return MLA_ERR_NULL;
+    if ((s = check_cache(dims, cache))) return s;
+    if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    const int splits = plan_splits(dims, cache, num_splits);
+    if (ws_bytes < attn_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dims->B == 0) return MLA_OK;
+    if (!q_cat || !o_lat || !lse) return MLA_ERR_NULL;
+    if (!aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse)) return MLA_ERR_ALIGN;
+
+    mla::AttnParams p = make_params(dims, cache);
+    p.q_cat = (const __nv_bfloat16 *)q_cat;
+    p.o_lat = (__nv_bfloat16 *)o_lat;
+    p.lse = lse;
+    p.num_splits = splits;
+    p.status = (int *)workspace;
+    if (splits > 1) {
+        size_t rows = (size_t)dims->B * splits * dims->s_q * dims->H;
+        char *base = (char *)workspace + kStatusBytes;
+        p.part_ml = (float *)base;
+        p.part_acc = (float *)(base + round_up(rows * 2 * sizeof(float), 256));
+    }
+    cudaError_t e = mla::launch_attn_simple(p, st);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_uv, void *out, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    if (dims->B == 0) return MLA_OK;
+    if (!o_lat || !w_uv || !out) return MLA_ERR_NULL;
+    if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGN;
+    cudaError_t e = mla::launch_out_proj_simple(*dims, o_lat, w_uv, out, as_stream(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API size_t mla_naive_workspace_size(const mla_dims *dims, const mla_cache *cache) {
+    if (check_dims(dims) || check_cache(dims, cache)) return 0;
+    size_t per = (size_t)dims->B * dims->H * (size_t)cache_capacity(cache);
+    return kStatusBytes + round_up(per * dims->d_nope * 2, 256) + per * dims->d_v * 2;
+}
+
+MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const void *q_rope,
+                             const mla_cache *cache, const void *w_uk, const void *w_uv, void *out, float *lse,
+                             void *workspace, size_t ws_bytes, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    if (!cache) return MLA_ERR_NULL;
+    if ((s = check_cache(dims, cache))) return s;
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    if (ws_bytes < mla_naive_workspace_size(dims, cache)) return MLA_ERR_WORKSPACE;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dims->B == 0) return MLA_OK;
+    if (!q_nope || !w_uk || !w_uv || !out || !lse || (dims->d_rope && !q_rope)) return MLA_ERR_NULL;
+    if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(out) || !aligned16(lse) ||
+        (q_rope && !aligned16(q_rope)))
+        return MLA_ERR_ALIGN;
+    mla::AttnParams p = make_params(dims, cache);
+    p.status = (int *)workspace;
+    size_t per = (size_t)dims->B * dims->H * (size_t)cache_capacity(cache);
+    char *kbuf = (char *)workspace + kStatusBytes;
+    (void)per;
+    cudaError_t e = mla::launch_naive(p, dims->d_nope, dims->d_v, q_nope, q_rope, w_uk, w_uv, out, lse, kbuf, st);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API int mla_read_status(const void *workspace, int *status, void *stream) {
+    if (!workspace || !status) return MLA_ERR_NULL;
+    int v = 0;
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+    *status = v;
+    return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// Shared device helpers of the MLA decode library (no method arithmetic here).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Parameters every attention kernel receives (plain values and device pointers).
+struct AttnParams {
+    int B, H, s_q, d_c, d_rope;
+    float scale;
+    const __nv_bfloat16 *q_cat;   // [B][s_q][H][W]
+    const __nv_bfloat16 *kv;      // contiguous or pool, rows of W
+    long long seq_stride;         // contiguous: elements between sequences
+    int capacity;                 // tokens a sequence may hold
+    const int *block_table;       // NULL => contiguous
+    int max_pages, page_size, num_pages;
+    const int *seq_lens;
+    __nv_bfloat16 *o_lat;         // [B][s_q][H][d_c]
+    float *lse;                   // [B][s_q][H]
+    int num_splits;
+    float *part_acc;              // [B][splits][s_q*H][d_c] (num_splits > 1)
+    float *part_ml;               // [B][splits][s_q*H][2]   (m, l)
+    int *status;                  // device status word
+};
+
+// Record the first device-side error; later ones keep the first.
+__device__ __forceinline__ void set_status(int *status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Whether sequence b's length is usable; records MLA_ERR_SEQLEN otherwise.
+__device__ __forceinline__ bool seq_len_ok(const AttnParams &p, int L) {
+    return L >= p.s_q && L <= p.capacity;
+}
+
+// Row of cached token j of sequence b, or nullptr if its page id is out of range.
+__device__ __forceinline__ const __nv_bfloat16 *kv_row(const AttnParams &p, int b, int j) {
+    const long long W = p.d_c + p.d_rope;
+    if (p.block_table == nullptr) return p.kv + (long long)b * p.seq_stride + (long long)j * W;
+    int page = __ldg(p.block_table + (long long)b * p.max_pages + j / p.page_size);
+    if (page < 0 || page >= p.num_pages) return nullptr;
+    return p.kv + ((long long)page * p.page_size + j % p.page_size) * W;
+}
+
+// Token range [t0, t1) of split `split` for a history of L tokens: the
+// ceil(L/64) 64-token tiles are dealt out in equal contiguous runs.
+__device__ __forceinline__ void split_range(int L, int splits, int split, int &t0, int &t1) {
+    int tiles = (L + 63) / 64;
+    int per = (tiles + splits - 1) / splits;
+    t0 = min(L, split * per * 64);
+    t1 = min(L, (split + 1) * per * 64);
+}
+
+}  // namespace mla

@@ -1,0 +1,103 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every symbol
+include/mla.h declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_decode_attention_absorbed_gb300 import build, mla
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return mla.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_symbols())
+    for n in ("mla_absorb_q", "mla_decode_attn", "mla_out_proj", "mla_naive_decode", "mla_decode_workspace_size"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(mla.EXPORTS)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.mla_abi_version() == 1
+    for code in range(10):
+        assert lib.mla_status_string(code).decode().startswith("MLA_")
+    assert lib.mla_status_string(99).decode() == "unknown mla status"
+
+
+def dsv3(B=4, s_q=1):
+    return mla.Problem(B, 128, s_q, 512, 64, 128, 128, 192 ** -0.5)
+
+
+def fake_cache(T=4096, paged=False):
+    # addresses are never dereferenced: these calls fail or size on the host only
+    kv, lens = 0x10000, 0x20000
+    if paged:
+        return mla.Cache(kv, 0, 0, 0x30000, T // 64, 64, 1000, lens, 0)
+    return mla.Cache(kv, T * 576, T, None, 0, 64, 0, lens, 0)
+
+
+def test_host_validation_without_gpu(lib):
+    d = dsv3().dims()
+    c = fake_cache()
+    nul = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(0x40000)
+    # NULL dims / pointers
+    assert lib.mla_absorb_q(None, a, a, a, a, nul) == 1
+    assert lib.mla_absorb_q(ctypes.byref(d), nul, a, a, a, nul) == 1
+    # misaligned pointer
+    assert lib.mla_absorb_q(ctypes.byref(d), ctypes.c_void_p(0x40008), a, a, a, nul) == 4
+    # unsupported shapes
+    for bad in (dict(d_c=96), dict(d_c=1024), dict(d_rope=8), dict(d_nope=24), dict(d_v=512), dict(H=4097)):
+        p = dsv3()
+        for k, v in bad.items():
+            setattr(p, k, v)
+        dd = p.dims()
+        assert lib.mla_absorb_q(ctypes.byref(dd), a, a, a, a, nul) == 6, bad
+    # negative sizes
+    p = dsv3()
+    p.B = -1
+    dd = p.dims()
+    assert lib.mla_out_proj(ctypes.byref(dd), a, a, a, nul) == 2
+    # decode: workspace too small, bad split count, bad cache
+    need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 4)
+    assert need > 256
+    assert lib.mla_decode_attn(ctypes.byref(d), a, ctypes.byref(c), a, a, a, need - 16, 4, nul) == 5
+    assert lib.mla_decode_attn(ctypes.byref(d), a, ctypes.byref(c), a, a, a, need, 65, nul) == 2
+    assert lib.mla_decode_attn(ctypes.byref(d), a, None, a, a, a, need, 4, nul) == 1
+    bad_stride = mla.Cache(0x10000, 100, 4096, None, 0, 64, 0, 0x20000, 0)
+    assert lib.mla_decode_attn(ctypes.byref(d), a, ctypes.byref(bad_stride), a, a, a, need, 4, nul) == 2
+    odd_page = mla.Cache(0x10000, 0, 0, 0x30000, 64, 32, 100, 0x20000, 0)
+    assert lib.mla_decode_attn(ctypes.byref(d), a, ctypes.byref(odd_page), a, a, a, need, 4, nul) == 6
+    assert lib.mla_read_status(None, None, nul) == 1
+
+
+def test_workspace_and_split_queries(lib):
+    d = dsv3(B=64).dims()
+    for paged in (False, True):
+        c = fake_cache(4096, paged)
+        s = lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c))
+        assert 1 <= s <= 64
+        one = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 1)
+        four = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 4)
+        assert one >= 4 and four >= 64 * 4 * 128 * 512 * 4
+    assert lib.mla_decode_workspace_size(None, None, 0) == 0
+    naive = lib.mla_naive_workspace_size(ctypes.byref(d), ctypes.byref(fake_cache(4096)))
+    assert naive >= 64 * 128 * 4096 * 256 * 2

@@ -1,0 +1,173 @@
+"""Parity of the CUDA path with the fp64 oracle, per output tensor, within
+max|gpu - ref| <= 2e-2 * max|ref| + 1e-3 (bf16 inputs, fp32 accumulation).
+
+Small cases are compared element by element on every row; the full-size
+workloads run in the launch configuration the benchmark times (automatic split
+count) and are compared on sampled rows the oracle computes one by one."""
+import pytest
+import torch
+
+import oracle
+from mla_decode_attention_absorbed_gb300 import mla
+from mla_decode_attention_absorbed_gb300.workloads import CONFIGS, MLAConfig, make_inputs
+
+from helpers import check_against_oracle, gpu_cache, run_gpu, sample_rows, to_dev, within_tolerance
+
+pytestmark = pytest.mark.gpu
+
+DSV3_DIMS = dict(H=128, d_c=512, d_rope=64, d_nope=128, d_v=128)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from mla_decode_attention_absorbed_gb300 import build
+    build.build()
+    mla.load()
+
+
+def test_tiny_config_all_rows():
+    cfg = CONFIGS["tiny"]
+    inp = make_inputs(cfg)
+    g = run_gpu(cfg, inp)
+    assert g["status"] == 0
+    check_against_oracle(cfg, inp, g)
+
+
+# several 64-token tiles, ragged tails, s_q 1/2/4, paged and contiguous, split counts
+CASES = [
+    ("contig_sq1", MLAConfig("c1", B=3, s_q=1, len_lo=65, len_hi=700, **DSV3_DIMS), 0),
+    ("contig_sq1_split1", MLAConfig("c1", B=3, s_q=1, len_lo=65, len_hi=700, **DSV3_DIMS), 1),
+    ("contig_sq1_split7", MLAConfig("c1", B=3, s_q=1, len_lo=65, len_hi=700, **DSV3_DIMS), 7),
+    ("contig_sq2", MLAConfig("c2", B=2, s_q=2, len_lo=100, len_hi=400, seed=3, **DSV3_DIMS), 2),
+    ("contig_sq4", MLAConfig("c4", B=2, s_q=4, len_lo=4, len_hi=300, seed=4, **DSV3_DIMS), 3),
+    ("paged_sq2", MLAConfig("p2", B=3, s_q=2, len_lo=2, len_hi=500, paged=True, seed=5, **DSV3_DIMS), 0),
+    ("paged_sq1_split5", MLAConfig("p1", B=2, s_q=1, len_lo=1, len_hi=900, paged=True, seed=6, **DSV3_DIMS), 5),
+    ("small_dims", MLAConfig("sd", B=3, H=16, d_c=64, d_rope=16, d_nope=32, d_v=32, s_q=3, len_lo=3,
+                             len_hi=300, seed=7), 2),
+    ("mid_dims", MLAConfig("md", B=2, H=40, d_c=192, d_rope=32, d_nope=64, d_v=48, s_q=2, len_lo=70,
+                           len_hi=260, seed=8), 0),
+]
+
+
+@pytest.mark.parametrize("name,cfg,splits", CASES, ids=[c[0] for c in CASES])
+def test_parity_small(name, cfg, splits):
+    inp = make_inputs(cfg)
+    g = run_gpu(cfg, inp, num_splits=splits)
+    assert g["status"] == 0
+    check_against_oracle(cfg, inp, g)
+
+
+def test_edge_lengths():
+    """L = s_q (every token new), L = 1, L on a tile boundary, L = capacity."""
+    cfg = MLAConfig("e", B=5, s_q=1, T=256, **DSV3_DIMS)
+    inp = make_inputs(cfg, seq_lens=[1, 64, 65, 255, 256])
+    check_against_oracle(cfg, inp, run_gpu(cfg, inp))
+    cfg4 = MLAConfig("e4", B=3, s_q=4, T=130, **DSV3_DIMS)
+    inp4 = make_inputs(cfg4, seq_lens=[4, 68, 130])
+    check_against_oracle(cfg4, inp4, run_gpu(cfg4, inp4, num_splits=2))
+
+
+def test_more_splits_than_tiles():
+    cfg = MLAConfig("e", B=2, s_q=2, T=100, **DSV3_DIMS)
+    inp = make_inputs(cfg, seq_lens=[70, 100])
+    check_against_oracle(cfg, inp, run_gpu(cfg, inp, num_splits=9))
+
+
+def test_split_counts_agree():
+    cfg = MLAConfig("s", B=2, s_q=1, T=2000, **DSV3_DIMS)
+    inp = make_inputs(cfg, seq_lens=[1999, 1333])
+    base = run_gpu(cfg, inp, num_splits=1)
+    for s in (2, 7, 64):
+        g = run_gpu(cfg, inp, num_splits=s)
+        within_tolerance(g["o_lat"], base["o_lat"].double(), f"o_lat splits={s}", rel=1e-2, abs_=1e-3)
+        within_tolerance(g["lse"], base["lse"].double(), f"lse splits={s}", rel=1e-4, abs_=1e-4)
+
+
+def test_paged_equals_contiguous_and_strided():
+    cfg = MLAConfig("pc", B=3, s_q=2, T=300, **DSV3_DIMS)
+    inp = make_inputs(cfg, seq_lens=[300, 131, 64])
+    ref = run_gpu(cfg, inp, num_splits=2)
+    # same tokens in shuffled 64-token pages
+    pages, table = [], []
+    for b, L in enumerate(inp["seq_lens"].tolist()):
+        ids = []
+        for p0 in range(0, L, 64):
+            blk = torch.full((64, cfg.W), float("nan"), dtype=torch.bfloat16)
+            take = inp["kv"][b, p0:min(L, p0 + 64)]
+            blk[:take.shape[0]] = take
+            ids.append(len(pages))
+            pages.append(blk)
+        table.append(ids)
+    perm = torch.randperm(len(pages), generator=torch.Generator().manual_seed(11))
+    pool = torch.stack(pages)[torch.argsort(perm)]
+    bt = torch.full((cfg.B, 6), -1, dtype=torch.int32)
+    for b, ids in enumerate(table):
+        bt[b, :len(ids)] = perm[torch.tensor(ids)].to(torch.int32)
+    pinp = dict(inp, kv=pool, block_table=bt)
+    pcfg = cfg.with_(paged=True)
+    g = run_gpu(pcfg, pinp, num_splits=2)
+    assert torch.equal(g["o_lat"], ref["o_lat"]) and torch.equal(g["lse"], ref["lse"])
+    # a contiguous cache whose sequences sit further apart than T_max rows
+    big = torch.full((cfg.B, 400, cfg.W), float("nan"), dtype=torch.bfloat16)
+    big[:, :300] = inp["kv"]
+    sinp = dict(inp, kv=big[:, :300])
+    g2 = run_gpu(cfg, sinp, num_splits=2)
+    assert torch.equal(g2["o_lat"], ref["o_lat"]) and torch.equal(g2["out"], ref["out"])
+
+
+def test_deterministic():
+    cfg = MLAConfig("d", B=2, s_q=2, T=500, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    a, b = run_gpu(cfg, inp, num_splits=3), run_gpu(cfg, inp, num_splits=3)
+    for k in ("q_cat", "o_lat", "lse", "out"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_empty_batch():
+    cfg = MLAConfig("z", B=0, s_q=1, T=64, **DSV3_DIMS)
+    prob = mla.Problem.of(cfg)
+    kv = torch.zeros(1, 64, cfg.W, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cache = mla.make_cache(prob, kv, lens)
+    q = torch.zeros(1, 1, 128, 576, dtype=torch.bfloat16, device="cuda")
+    o, lse, ws = mla.decode_attn(prob, q, cache)
+    assert mla.read_status(ws) == 0
+
+
+# ---------------------------------------------------------------- full-size workloads, sampled rows
+@pytest.mark.parametrize("name", ["dsv3", "long", "spec", "ragged_paged"])
+def test_full_size_sampled(name):
+    cfg = CONFIGS[name]
+    inp = make_inputs(cfg)
+    g = run_gpu(cfg, inp)
+    assert g["status"] == 0
+    rows = sample_rows(cfg, 48)
+    check_against_oracle(cfg, inp, g, rows=rows)
+    for k in ("o_lat", "lse", "out"):
+        assert torch.isfinite(g[k].float()).all(), k
+
+
+# ---------------------------------------------------------------- naive comparison path
+def _run_naive(cfg, inp):
+    d = to_dev(inp)
+    prob, cache = gpu_cache(cfg, d)
+    out, lse, ws = mla.naive_decode(prob, d["q_nope"], d["q_rope"], cache, d["w_uk"], d["w_uv"])
+    st = mla.read_status(ws)
+    return out.cpu(), lse.cpu(), st
+
+
+@pytest.mark.parametrize("cfg", [CONFIGS["tiny"],
+                                 MLAConfig("n", B=2, s_q=2, len_lo=60, len_hi=300, seed=2, **DSV3_DIMS),
+                                 MLAConfig("np", B=2, s_q=1, len_lo=60, len_hi=300, paged=True, seed=9,
+                                           **DSV3_DIMS)], ids=["tiny", "dsv3dims", "paged"])
+def test_naive_path_matches_oracle(cfg):
+    inp = make_inputs(cfg)
+    out, lse, st = _run_naive(cfg, inp)
+    assert st == 0
+    ref_out, ref_lse = oracle.naive(cfg, inp["q_nope"], inp["q_rope"], inp["kv"], inp["seq_lens"],
+                                    inp["w_uk"], inp["w_uv"], inp["block_table"], cfg.page_size)
+    within_tolerance(out, ref_out, "naive out")
+    within_tolerance(lse, ref_lse, "naive lse")
+    # and the absorbed GPU path agrees with it
+    g = run_gpu(cfg, inp)
+    within_tolerance(g["out"], ref_out, "absorbed vs naive reference")
