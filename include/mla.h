@@ -164,6 +164,32 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
                              void *out, float *lse, void *workspace, size_t ws_bytes,
                              void *stream);
 
+/* mla_decode_attn for callers that cannot allocate scratch memory.  The pages
+ * have no counterpart of this entry point; it exists for hosts that hold only
+ * their input and output buffers, such as a plain C or FFI caller with no
+ * device allocator, or a serving loop whose device memory belongs to a
+ * framework pool and where a cudaMalloc (which may synchronise the device) is
+ * not allowed while decoding.
+ * Same computation, arguments and outputs as mla_decode_attn, without the
+ * workspace: the status word and the split partials live in one 32 MiB array
+ * compiled into the library (a file-scope __device__ array; every GPU on which
+ * the library's kernels are loaded holds it until the process exits).  Nothing
+ * is allocated or freed by this call.
+ *  - The first call on each device looks the array's device address up once
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - num_splits 0 takes the library's split count if its partials fit in the
+ *    array, else the largest count that fits (1 always fits).  An explicit
+ *    num_splits whose partials exceed 32 MiB returns MLA_ERR_WORKSPACE.
+ *  - Every call shares the one array and overwrites it: calls that overlap on
+ *    the GPU (other streams, other host threads, without ordering between them)
+ *    race and corrupt each other's results.  Order them on one stream.
+ *  - device_status (optional, device int32): receives this call's device status
+ *    word (as mla_read_status would report it) once the call has run. */
+MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
+                                    void *o_lat, float *lse, int num_splits, int *device_status,
+                                    void *stream);
+
 /* Wait for `stream`, then copy the device status word at the start of
  * `workspace` (written by the last mla_decode_attn / mla_naive_decode that used
  * it) into *status: MLA_OK, MLA_ERR_SEQLEN, MLA_ERR_PAGE or MLA_ERR_TIMEOUT.

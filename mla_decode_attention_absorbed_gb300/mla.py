@@ -37,7 +37,7 @@ class Cache(ctypes.Structure):
 
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_workspace_size",
            "mla_decode_num_splits", "mla_decode_attn", "mla_out_proj", "mla_naive_workspace_size",
-           "mla_naive_decode", "mla_read_status")
+           "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc")
 
 
 def lib_path() -> str:
@@ -74,6 +74,8 @@ def load(path: str | None = None):
     lib.mla_naive_decode.restype = I
     lib.mla_read_status.argtypes = [P, ctypes.POINTER(I), P]
     lib.mla_read_status.restype = I
+    lib.mla_decode_attn_noalloc.argtypes = [pd, P, pc, P, P, I, P, P]
+    lib.mla_decode_attn_noalloc.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -216,6 +218,17 @@ def naive_decode(prob: Problem, q_nope, q_rope, cache: Cache, w_uk, w_uv, out=No
                                 _ptr(w_uv), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                 _stream(stream)), "mla_naive_decode")
     return out, lse, workspace
+
+
+def decode_attn_noalloc(prob: Problem, q_cat, cache: Cache, o_lat, lse, num_splits: int = 0,
+                        device_status=None, stream=None):
+    """mla_decode_attn_noalloc: the same attention with the library's built-in
+    scratch array instead of a workspace (for callers that cannot allocate)."""
+    d = prob.dims()
+    _check(load().mla_decode_attn_noalloc(ctypes.byref(d), _ptr(q_cat), ctypes.byref(cache), _ptr(o_lat),
+                                          _ptr(lse), int(num_splits), _ptr(device_status), _stream(stream)),
+           "mla_decode_attn_noalloc")
+    return o_lat, lse
 
 
 def read_status(workspace, stream=None) -> int:
