@@ -29,8 +29,9 @@
  *    reports a failed launch.  Problems only the device can see (a sequence
  *    length or block-table entry out of range, a bounded wait that ran out) are
  *    written to the status word at the start of the workspace; read it with
- *    mla_read_status.  The affected sequence's outputs are written as zeros
- *    (lse = -inf); nothing faults and nothing reads outside the caller's buffers.
+ *    mla_read_status.  A sequence with an invalid length gets zero outputs and
+ *    lse = -inf; tokens on a page outside the pool are skipped.  Nothing faults
+ *    and nothing reads outside the caller's buffers.
  *  - Dimensions: H >= 1, s_q >= 1, d_c a multiple of 64 up to 512, d_rope a
  *    multiple of 16 up to 64, d_nope and d_v multiples of 16 from 16 to 256,
  *    s_q * H <= 4096.  Other shapes return MLA_ERR_UNSUPPORTED.

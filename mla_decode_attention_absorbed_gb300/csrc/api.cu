@@ -122,7 +122,7 @@ MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q
     if (!q_nope || !w_uk || !q_cat || (dims->d_rope && !q_rope)) return MLA_ERR_NULL;
     if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_cat) || (q_rope && !aligned16(q_rope)))
         return MLA_ERR_ALIGN;
-    cudaError_t e = mla::launch_absorb_q_simple(*dims, q_nope, q_rope, w_uk, q_cat, as_stream(stream));
+    cudaError_t e = mla::launch_absorb_q_tc(*dims, q_nope, q_rope, w_uk, q_cat, as_stream(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -148,11 +148,13 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     const int splits = plan_splits(dims, cache, num_splits);
     if (ws_bytes < attn_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    if (dims->B > 0) {
+        if (!q_cat || !o_lat || !lse) return MLA_ERR_NULL;
+        if (!aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse)) return MLA_ERR_ALIGN;
+    }
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
     if (dims->B == 0) return MLA_OK;
-    if (!q_cat || !o_lat || !lse) return MLA_ERR_NULL;
-    if (!aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse)) return MLA_ERR_ALIGN;
 
     mla::AttnParams p = make_params(dims, cache);
     p.q_cat = (const __nv_bfloat16 *)q_cat;
@@ -166,7 +168,7 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
         p.part_ml = (float *)base;
         p.part_acc = (float *)(base + round_up(rows * 2 * sizeof(float), 256));
     }
-    cudaError_t e = mla::launch_attn_simple(p, st);
+    cudaError_t e = mla::launch_attn_tc(p, st);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -176,7 +178,7 @@ MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_
     if (dims->B == 0) return MLA_OK;
     if (!o_lat || !w_uv || !out) return MLA_ERR_NULL;
     if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_ALIGN;
-    cudaError_t e = mla::launch_out_proj_simple(*dims, o_lat, w_uv, out, as_stream(stream));
+    cudaError_t e = mla::launch_out_proj_tc(*dims, o_lat, w_uv, out, as_stream(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -196,18 +198,18 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     if (ws_bytes < mla_naive_workspace_size(dims, cache)) return MLA_ERR_WORKSPACE;
+    if (dims->B > 0) {
+        if (!q_nope || !w_uk || !w_uv || !out || !lse || (dims->d_rope && !q_rope)) return MLA_ERR_NULL;
+        if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(out) || !aligned16(lse) ||
+            (q_rope && !aligned16(q_rope)))
+            return MLA_ERR_ALIGN;
+    }
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
     if (dims->B == 0) return MLA_OK;
-    if (!q_nope || !w_uk || !w_uv || !out || !lse || (dims->d_rope && !q_rope)) return MLA_ERR_NULL;
-    if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(out) || !aligned16(lse) ||
-        (q_rope && !aligned16(q_rope)))
-        return MLA_ERR_ALIGN;
     mla::AttnParams p = make_params(dims, cache);
     p.status = (int *)workspace;
-    size_t per = (size_t)dims->B * dims->H * (size_t)cache_capacity(cache);
     char *kbuf = (char *)workspace + kStatusBytes;
-    (void)per;
     cudaError_t e = mla::launch_naive(p, dims->d_nope, dims->d_v, q_nope, q_rope, w_uk, w_uv, out, lse, kbuf, st);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -1,0 +1,226 @@
+// Per-head projection GEMMs on the 5th-generation tensor cores (tcgen05):
+//   absorb:  q_cat[m,h,0:d_c] = q_nope[m,h,:] . W_UK[h]^T          (B operand K-major)
+//   out:     out[m,h,:]       = o_lat[m,h,:]  . W_UV[h]            (B operand MN-major)
+// ("MLA, dim by dim", "MLA Decode": absorb W_UK^T into the current query, and
+// apply W_UV once to the latent-space output.)  m = b*s_q + i runs over the
+// batch's query tokens; one CTA computes a 128-row x BN-column tile of one head.
+//
+// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns tensor memory
+// and issues the MMAs, warps 2-5 drain the fp32 accumulator from TMEM, round to
+// bf16 and store.  K is streamed in 64-wide chunks through a 4-stage ring.
+#include "common.cuh"
+#include "launch.h"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+
+struct ProjArgs {
+    int M;                 // query tokens (B * s_q)
+    int H;                 // heads = batch of the GEMM
+    int N;                 // output width per head
+    int K;                 // contraction width
+    __nv_bfloat16 *out;    // row m, head h, column n at out + (m*H + h)*out_row + n
+    int out_row;           // elements per (m, h) output row
+    const __nv_bfloat16 *rope_src;  // absorb only: q_rope [M][H][d_rope], copied after column d_c
+    int d_rope;
+};
+
+template <int BN>
+struct ProjSmem {
+    static constexpr uint32_t kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+    static constexpr int kBBytes = BN * kBK * 2;   // 32 KB at BN = 256
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBytes = kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+};
+
+template <int BN, bool kBMN>
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, ProjArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment: the 128-byte swizzle pattern repeats every 8 rows of 128 B
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = ProjSmem<BN>;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * L::kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *acc_full = empty + kStages;
+    uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_slot + 1);
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM, h = blockIdx.z;
+    const int nk = (g.K + kBK - 1) / kBK;  // the last chunk's columns past K read as zero
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc<L::kTmemCols>(tmem_base_slot);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        for (int kc = 0; kc < nk; ++kc) {
+            const int s = kc % kStages;
+            if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            uint8_t *sa = smem + s * L::kStageBytes;
+            uint8_t *sb = sa + L::kABytes;
+            mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+            tma_load_3d(sa, &tmA, &full[s], kc * kBK, h, m0);
+            if (kBMN) {
+                for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tmB, &full[s], n0 + 64 * j, kc * kBK, h);
+            } else {
+                tma_load_3d(sb, &tmB, &full[s], kc * kBK, n0, h);
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16(kBM, BN, false, kBMN);
+        bool ok = true;
+        for (int kc = 0; kc < nk && ok; ++kc) {
+            const int s = kc % kStages;
+            if (!mbar_wait(&full[s], (kc / kStages) & 1)) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + s * L::kStageBytes);
+            const uint32_t sb = sa + L::kABytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                const uint64_t da = smem_desc_sw128(sa + kk * 32, 16, 1024);
+                const uint64_t db = kBMN ? smem_desc_sw128(sb + kk * 16 * 128, 64 * 128, 1024)
+                                         : smem_desc_sw128(sb + kk * 32, 16, 1024);
+                mma_ss(tmem, da, db, idesc, (kc | kk) != 0);
+            }
+            mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        }
+        mma_commit(acc_full);
+    } else if (warp >= 2) {
+        // ---------------- epilogue: TMEM -> bf16 -> global
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = q * 32 + lane;
+        const int m = m0 + row;
+        const bool ok = mbar_wait(acc_full, 0) && !*abort_flag;
+        tc_fence_after();
+        __nv_bfloat16 *dst = g.out + ((long long)m * g.H + h) * g.out_row + n0;
+        const int n_valid = g.N - n0;  // a multiple of 16
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tmem + tmem_lane_base(q) + c0, r);
+            tmem_ld_wait();
+            if (m < g.M && c0 < n_valid) {
+                uint32_t pk[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    float lo = ok ? __uint_as_float(r[2 * e]) : __int_as_float(0x7fc00000);
+                    float hi = ok ? __uint_as_float(r[2 * e + 1]) : __int_as_float(0x7fc00000);
+                    pk[e] = pack_bf16x2(lo, hi);
+                }
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+                d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+        }
+        if (g.rope_src != nullptr && blockIdx.x == 0 && m < g.M) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(g.rope_src + ((long long)m * g.H + h) * g.d_rope);
+            uint4 *d = reinterpret_cast<uint4 *>(g.out + ((long long)m * g.H + h) * g.out_row + g.N);
+            for (int e = 0; e < g.d_rope / 8; ++e) d[e] = src[e];
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_free<L::kTmemCols>(tmem);
+    }
+}
+
+template <int BN, bool kBMN>
+cudaError_t launch_proj(const CUtensorMap &tA, const CUtensorMap &tB, const ProjArgs &g, cudaStream_t st) {
+    const int smem = ProjSmem<BN>::kBytes;
+    cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<BN, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((g.N + BN - 1) / BN, (g.M + kBM - 1) / kBM, g.H);
+    proj_gemm_tc<BN, kBMN><<<grid, kThreads, smem, st>>>(tA, tB, g);
+    return cudaGetLastError();
+}
+
+// A operand [M][H][K] bf16 (K contiguous), box 64 x 1 x 128.
+bool map_rows(CUtensorMap *m, const void *base, int M, int H, int K) {
+    uint64_t dims[3] = {(uint64_t)K, (uint64_t)H, (uint64_t)M};
+    uint64_t strides[2] = {(uint64_t)K * 2, (uint64_t)H * K * 2};
+    uint32_t box[3] = {64, 1, kBM};
+    return encode_bf16_sw128(m, base, 3, dims, strides, box);
+}
+
+}  // namespace
+
+// q_cat = [q_nope . W_UK^T | q_rope]
+cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void *q_rope, const void *w_uk,
+                               void *q_cat, cudaStream_t st) {
+    const int M = d.B * d.s_q;
+    CUtensorMap tA, tB;
+    if (!map_rows(&tA, q_nope, M, d.H, d.d_nope)) return cudaErrorInvalidValue;
+    // W_UK [H][d_c][d_nope]: K-major B, box 64 (k) x BN (n) x 1
+    const int BN = d.d_c >= 256 ? 256 : d.d_c;  // d_c is a multiple of 64
+    uint64_t dims[3] = {(uint64_t)d.d_nope, (uint64_t)d.d_c, (uint64_t)d.H};
+    uint64_t strides[2] = {(uint64_t)d.d_nope * 2, (uint64_t)d.d_c * d.d_nope * 2};
+    uint32_t box[3] = {64, (uint32_t)BN, 1};
+    if (!encode_bf16_sw128(&tB, w_uk, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    ProjArgs g{M, d.H, d.d_c, d.d_nope, (__nv_bfloat16 *)q_cat, d.d_c + d.d_rope,
+               d.d_rope ? (const __nv_bfloat16 *)q_rope : nullptr, d.d_rope};
+    switch (BN) {
+        case 256: return launch_proj<256, false>(tA, tB, g, st);
+        case 192: return launch_proj<192, false>(tA, tB, g, st);
+        case 128: return launch_proj<128, false>(tA, tB, g, st);
+        case 64: return launch_proj<64, false>(tA, tB, g, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// out = o_lat . W_UV
+cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void *w_uv, void *out, cudaStream_t st) {
+    const int M = d.B * d.s_q;
+    CUtensorMap tA, tB;
+    if (!map_rows(&tA, o_lat, M, d.H, d.d_c)) return cudaErrorInvalidValue;
+    // W_UV [H][d_c][d_v]: MN-major B, box 64 (n) x 64 (k) x 1
+    uint64_t dims[3] = {(uint64_t)d.d_v, (uint64_t)d.d_c, (uint64_t)d.H};
+    uint64_t strides[2] = {(uint64_t)d.d_v * 2, (uint64_t)d.d_c * d.d_v * 2};
+    uint32_t box[3] = {64, 64, 1};
+    if (!encode_bf16_sw128(&tB, w_uv, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    ProjArgs g{M, d.H, d.d_v, d.d_c, (__nv_bfloat16 *)out, d.d_v, nullptr, 0};
+    switch ((d.d_v + 63) / 64 * 64) {  // MMA width: d_v rounded up to whole 64-column boxes
+        case 256: return launch_proj<256, true>(tA, tB, g, st);
+        case 192: return launch_proj<192, true>(tA, tB, g, st);
+        case 128: return launch_proj<128, true>(tA, tB, g, st);
+        case 64: return launch_proj<64, true>(tA, tB, g, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace mla

@@ -1,84 +1,9 @@
-// Straightforward CUDA-core kernels for the absorbed decode step: correct by
-// construction, used to stand the boundary up.  The tensor-core kernels replace
-// them on the timed path.
+// CUDA-core split attention (the first, correctness-first version) and the
+// cross-split log-sum-exp combine.
 #include "common.cuh"
 #include "launch.h"
 
 namespace mla {
-
-// ----------------------------------------------------------------------------
-// q_cat[m,h,0:d_c] = q_nope[m,h,:] . W_UK[h,c,:];  q_cat[m,h,d_c:] = q_rope[m,h,:]
-// ("MLA, dim by dim", MLA Decode: absorb W_UK^T into the current query).
-// grid (H, ceil(M/16)), 256 threads; m = b*s_q + i.
-// ----------------------------------------------------------------------------
-constexpr int kProjRows = 16;
-
-__global__ void absorb_q_simple(int M, int H, int d_c, int d_rope, int d_nope,
-                                const __nv_bfloat16 *__restrict__ q_nope,
-                                const __nv_bfloat16 *__restrict__ q_rope,
-                                const __nv_bfloat16 *__restrict__ w_uk,
-                                __nv_bfloat16 *__restrict__ q_cat) {
-    __shared__ float qs[kProjRows][256];
-    const int h = blockIdx.x, m0 = blockIdx.y * kProjRows;
-    const int W = d_c + d_rope;
-    for (int e = threadIdx.x; e < kProjRows * d_nope; e += blockDim.x) {
-        int r = e / d_nope, n = e % d_nope;
-        int m = m0 + r;
-        qs[r][n] = m < M ? __bfloat162float(q_nope[((long long)m * H + h) * d_nope + n]) : 0.f;
-    }
-    __syncthreads();
-    for (int c = threadIdx.x; c < d_c; c += blockDim.x) {
-        float acc[kProjRows];
-#pragma unroll
-        for (int r = 0; r < kProjRows; ++r) acc[r] = 0.f;
-        const __nv_bfloat16 *wrow = w_uk + ((long long)h * d_c + c) * d_nope;
-        for (int n = 0; n < d_nope; ++n) {
-            float w = __bfloat162float(wrow[n]);
-#pragma unroll
-            for (int r = 0; r < kProjRows; ++r) acc[r] += qs[r][n] * w;
-        }
-#pragma unroll
-        for (int r = 0; r < kProjRows; ++r) {
-            int m = m0 + r;
-            if (m < M) q_cat[((long long)m * H + h) * W + c] = __float2bfloat16_rn(acc[r]);
-        }
-    }
-    for (int e = threadIdx.x; e < kProjRows * d_rope; e += blockDim.x) {
-        int r = e / d_rope, k = e % d_rope;
-        int m = m0 + r;
-        if (m < M) q_cat[((long long)m * H + h) * W + d_c + k] = q_rope[((long long)m * H + h) * d_rope + k];
-    }
-}
-
-// out[m,h,v] = sum_c o_lat[m,h,c] W_UV[h,c,v]  ("MLA, dim by dim", decode value order).
-__global__ void out_proj_simple(int M, int H, int d_c, int d_v,
-                                const __nv_bfloat16 *__restrict__ o_lat,
-                                const __nv_bfloat16 *__restrict__ w_uv,
-                                __nv_bfloat16 *__restrict__ out) {
-    extern __shared__ float os[];  // [kProjRows][d_c]
-    const int h = blockIdx.x, m0 = blockIdx.y * kProjRows;
-    for (int e = threadIdx.x; e < kProjRows * d_c; e += blockDim.x) {
-        int r = e / d_c, c = e % d_c;
-        int m = m0 + r;
-        os[e] = m < M ? __bfloat162float(o_lat[((long long)m * H + h) * d_c + c]) : 0.f;
-    }
-    __syncthreads();
-    for (int v = threadIdx.x; v < d_v; v += blockDim.x) {
-        float acc[kProjRows];
-#pragma unroll
-        for (int r = 0; r < kProjRows; ++r) acc[r] = 0.f;
-        for (int c = 0; c < d_c; ++c) {
-            float w = __bfloat162float(w_uv[((long long)h * d_c + c) * d_v + v]);
-#pragma unroll
-            for (int r = 0; r < kProjRows; ++r) acc[r] += os[r * d_c + c] * w;
-        }
-#pragma unroll
-        for (int r = 0; r < kProjRows; ++r) {
-            int m = m0 + r;
-            if (m < M) out[((long long)m * H + h) * d_v + v] = __float2bfloat16_rn(acc[r]);
-        }
-    }
-}
 
 // ----------------------------------------------------------------------------
 // Split attention, one CTA per (row block of 16 query rows, split, sequence).
@@ -87,7 +12,6 @@ __global__ void out_proj_simple(int M, int H, int d_c, int d_v,
 // ----------------------------------------------------------------------------
 constexpr int kSR = 16;   // query rows per CTA
 constexpr int kST = 32;   // tokens per tile
-constexpr int kMaxW = 576;
 
 __global__ void __launch_bounds__(256) attn_split_simple(AttnParams p) {
     extern __shared__ float dyn[];
@@ -264,26 +188,6 @@ __global__ void attn_combine(AttnParams p) {
 }
 
 // ----------------------------------------------------------------------------
-cudaError_t launch_absorb_q_simple(const mla_dims &d, const void *q_nope, const void *q_rope,
-                                   const void *w_uk, void *q_cat, cudaStream_t st) {
-    int M = d.B * d.s_q;
-    dim3 grid(d.H, (M + kProjRows - 1) / kProjRows);
-    absorb_q_simple<<<grid, 256, 0, st>>>(M, d.H, d.d_c, d.d_rope, d.d_nope,
-                                          (const __nv_bfloat16 *)q_nope, (const __nv_bfloat16 *)q_rope,
-                                          (const __nv_bfloat16 *)w_uk, (__nv_bfloat16 *)q_cat);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_out_proj_simple(const mla_dims &d, const void *o_lat, const void *w_uv, void *out,
-                                   cudaStream_t st) {
-    int M = d.B * d.s_q;
-    dim3 grid(d.H, (M + kProjRows - 1) / kProjRows);
-    size_t smem = sizeof(float) * kProjRows * d.d_c;
-    out_proj_simple<<<grid, 128, smem, st>>>(M, d.H, d.d_c, d.d_v, (const __nv_bfloat16 *)o_lat,
-                                             (const __nv_bfloat16 *)w_uv, (__nv_bfloat16 *)out);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_attn_simple(const AttnParams &p, cudaStream_t st) {
     int rows = p.s_q * p.H;
     dim3 grid((rows + kSR - 1) / kSR, p.num_splits, p.B);
@@ -295,7 +199,12 @@ cudaError_t launch_attn_simple(const AttnParams &p, cudaStream_t st) {
     attn_split_simple<<<grid, 256, smem, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.num_splits == 1) return e;
-    attn_combine<<<(unsigned)((long long)p.B * rows), 128, 0, st>>>(p);
+    return launch_attn_combine(p, st);
+}
+
+cudaError_t launch_attn_combine(const AttnParams &p, cudaStream_t st) {
+    const long long rows = (long long)p.B * p.s_q * p.H;
+    attn_combine<<<(unsigned)rows, 128, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,8 +24,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // A wait longer than this is treated as lost: the caller records MLA_ERR_TIMEOUT
-// and unwinds instead of hanging the GPU.
+// and unwinds instead of hanging the GPU.  Two clocks bound it, the global
+// nanosecond timer and the SM cycle counter (4e9 cycles: ~2 s at 2 GHz), so the
+// limit holds even if one of them does not advance.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
+__device__ __forceinline__ bool wait_expired(uint64_t t0_ns, long long c0) {
+    return globaltimer_ns() - t0_ns > kWaitLimitNs || clock64() - c0 > kWaitLimitCycles;
+}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
@@ -79,9 +87,10 @@ template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
+    const long long c0 = clock64();
     for (uint32_t it = 1;; ++it) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 63u) == 0 && wait_expired(t0, c0)) return false;
     }
 }
 
