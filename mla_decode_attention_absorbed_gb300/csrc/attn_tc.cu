@@ -39,7 +39,7 @@ constexpr int kStages = 4;        // tiles in flight
 constexpr int kMaxBoxes = 5;      // 64-channel boxes per tile and CTA (320 channels)
 constexpr int kBoxBytes = kTile * 128;
 constexpr int kStageBytes = kMaxBoxes * kBoxBytes;  // 40 KB
-constexpr int kRxPitch = 68;      // floats per row of the partial-score exchange buffer
+constexpr int kXBytes = kRows * kTile * 4;  // one partial-score tile, fp32 (32 KB)
 constexpr int kThreads = 192;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
@@ -53,11 +53,16 @@ struct Geo {
 
 struct Smem {
     uint8_t kv[kStages][kStageBytes];
-    float rx[kRows * kRxPitch];  // the peer's partial scores (split mode)
+    // split mode: this CTA's partial scores staged for the bulk copy to the peer,
+    // and the peer's partial scores received.  Row r's 16-byte chunk c sits at
+    // chunk c ^ (r % 16), so that a warp's row-per-thread accesses do not collide.
+    float tx[kRows * kTile];
+    float rx[kRows * kTile];
     uint64_t full[kStages], empty[kStages];
     uint64_t q_ready, s_full, s_free, p_ready, o_done, rx_full, peer_rx_free, drain;
     uint32_t tmem_base;
-    int abort;
+    int abort;  // set by this CTA or, remotely, by the peer
+    int stop;   // the softmax warps' common decision to leave the tile loop
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -129,10 +134,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.s_free, 128);
         mbar_init(&sm.p_ready, 128);
         mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.rx_full, 128);
-        mbar_init(&sm.peer_rx_free, 128);
+        mbar_init(&sm.rx_full, 1);
+        mbar_init(&sm.peer_rx_free, 1);
         mbar_init(&sm.drain, 1);
         sm.abort = 0;
+        sm.stop = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_kv);
     }
@@ -282,59 +288,111 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         uint32_t rx_peer = 0, rxfull_peer = 0, rxfree_peer = 0;
         if (kSplit) {
-            rx_peer = map_to_rank(smem_u32(&sm.rx[r * kRxPitch]), peer);
+            rx_peer = map_to_rank(smem_u32(sm.rx), peer);
             rxfull_peer = map_to_rank(smem_u32(&sm.rx_full), peer);
             rxfree_peer = map_to_rank(smem_u32(&sm.peer_rx_free), peer);
         }
+        const int sw = r & 15;  // chunk swizzle of this row in tx / rx
 
         float m2 = -INFINITY;  // running (possibly stale) maximum, log2 units
         float l = 0.f;
         bool ok = true;
+        int armed = -1, received = -1;  // last receive this CTA armed / completed (split mode)
         for (int n = 0; n < ntiles; ++n) {
-            if (!warp_wait(sm, &sm.s_full, n & 1)) { ok = false; break; }
+            bool good = warp_wait(sm, &sm.s_full, n & 1);
             tc_fence_after();
             float s[kTile];
             {
-                uint32_t u[16];
+                uint32_t u0[16], u1[16], u2[16], u3[16];
+                tmem_ld16(tmem + lane_base + kColS + 0, u0);
+                tmem_ld16(tmem + lane_base + kColS + 16, u1);
+                tmem_ld16(tmem + lane_base + kColS + 32, u2);
+                tmem_ld16(tmem + lane_base + kColS + 48, u3);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kTile; c += 16) {
-                    tmem_ld16(tmem + lane_base + kColS + c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) s[c + e] = __uint_as_float(u[e]);
+                for (int e = 0; e < 16; ++e) {
+                    s[e] = __uint_as_float(u0[e]);
+                    s[16 + e] = __uint_as_float(u1[e]);
+                    s[32 + e] = __uint_as_float(u2[e]);
+                    s[48 + e] = __uint_as_float(u3[e]);
                 }
             }
             tc_fence_before();
             mbar_arrive(&sm.s_free);
             if (kSplit) {
-                // partial scores to the peer; the peer's partial back
-                if (n >= 1 && !warp_wait<true>(sm, &sm.peer_rx_free, (n - 1) & 1)) { ok = false; break; }
+                // Swap partial scores with the peer: stage locally, one bulk copy
+                // each way (completing bytes on the receiver's barrier), sum.
+                // Named barriers keep the 128 threads in step; nobody leaves the loop
+                // between them, and the decision to stop is taken jointly.
+                float4 *txrow = reinterpret_cast<float4 *>(sm.tx + r * kTile);
 #pragma unroll
-                for (int c = 0; c < kTile; c += 4) st_cluster_v4(rx_peer + c * 4, s[c], s[c + 1], s[c + 2], s[c + 3]);
-                mbar_arrive_remote(rxfull_peer);
-                if (!warp_wait<true>(sm, &sm.rx_full, n & 1)) { ok = false; break; }
-                const float4 *mine = reinterpret_cast<const float4 *>(&sm.rx[r * kRxPitch]);
+                for (int c = 0; c < kTile / 4; ++c)
+                    txrow[c ^ sw] = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+                fence_proxy_async_smem();
+                named_bar(1, 128);
+                if (threadIdx.x == 0) {
+                    bool go = !*(volatile int *)&sm.abort;
+                    if (go && n >= 1 && !wait_bar<true>(sm, &sm.peer_rx_free, (n - 1) & 1)) {
+                        raise_abort<kSplit>(sm, p, peer);
+                        go = false;
+                    }
+                    mbar_arrive_expect_tx(&sm.rx_full, kXBytes);  // arm this CTA's receive of tile n
+                    armed = n;
+                    if (go) {
+                        bulk_copy_to_peer(rx_peer, sm.tx, kXBytes, rxfull_peer);
+                        bulk_commit();
+                    }
+                }
+                if (warp_wait<true>(sm, &sm.rx_full, n & 1)) {
+                    if (threadIdx.x == 0) received = n;
+                } else {
+                    good = false;
+                }
+                const float4 *rxrow = reinterpret_cast<const float4 *>(sm.rx + r * kTile);
 #pragma unroll
                 for (int c = 0; c < kTile / 4; ++c) {
-                    float4 v = mine[c];
+                    const float4 v = rxrow[c ^ sw];
                     s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
                 }
-                mbar_arrive_remote(rxfree_peer);
+                if (!good) raise_abort<kSplit>(sm, p, peer);
+                if (threadIdx.x == 0) {
+                    bulk_wait_read_all();  // tx may be rewritten next tile
+                    sm.stop = *(volatile int *)&sm.abort;
+                }
+                named_bar(1, 128);
+                const bool stop = *(volatile int *)&sm.stop;
+                if (threadIdx.x == 0 && !stop) mbar_arrive_remote(rxfree_peer);  // the peer may refill rx
+                if (stop) {
+                    ok = false;
+                    break;
+                }
+            } else if (!good) {
+                ok = false;
+                break;
             }
-            // scale, mask, tile maximum
+            // scale, mask (only tiles that reach past a limit), tile maximum
             const int tok0 = t0 + n * kTile;
-            bool tile_ok = row_ok;
+            bool tile_ok = true;
             if (kPaged) {
                 const int page = __ldg(p.block_table + (long long)b * p.max_pages + tok0 / p.page_size);
-                tile_ok = tile_ok && page >= 0 && page < p.num_pages;  // tokens of a bad page are skipped
+                tile_ok = page >= 0 && page < p.num_pages;  // tokens of a bad page are skipped
             }
+            const bool whole = tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q;
             float tmax = -INFINITY;
+            if (whole) {
 #pragma unroll
-            for (int j = 0; j < kTile; ++j) {
-                const int tok = tok0 + j;
-                const bool vis = tile_ok && tok < t1 && tok <= lim;
-                s[j] = vis ? s[j] * scale_log2 : -INFINITY;
-                tmax = fmaxf(tmax, s[j]);
+                for (int j = 0; j < kTile; ++j) {
+                    s[j] *= scale_log2;
+                    tmax = fmaxf(tmax, s[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < kTile; ++j) {
+                    const int tok = tok0 + j;
+                    const bool vis = tile_ok && row_ok && tok < t1 && tok <= lim;
+                    s[j] = vis ? s[j] * scale_log2 : -INFINITY;
+                    tmax = fmaxf(tmax, s[j]);
+                }
             }
             float m_use = m2, alpha = 1.f;
             bool rescale = false;
@@ -347,18 +405,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float sum = 0.f;
             uint32_t pk[kTile / 2];
+            if (m_use == -INFINITY) {
 #pragma unroll
-            for (int j = 0; j < kTile; j += 2) {
-                const float a = m_use == -INFINITY ? 0.f : ex2(s[j] - m_use);
-                const float c = m_use == -INFINITY ? 0.f : ex2(s[j + 1] - m_use);
-                sum += a + c;
-                pk[j / 2] = pack_bf16x2(a, c);
+                for (int j = 0; j < kTile / 2; ++j) pk[j] = 0u;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kTile; j += 2) {
+                    const float a = ex2(s[j] - m_use);
+                    const float c = ex2(s[j + 1] - m_use);
+                    sum += a + c;
+                    pk[j / 2] = pack_bf16x2(a, c);
+                }
             }
             l = l * alpha + sum;
             m2 = m_use;
             // the previous P . V must be done before O is rescaled or P overwritten
             if (n >= 1) {
-                if (!warp_wait(sm, &sm.o_done, (n - 1) & 1)) { ok = false; break; }
+                if (!warp_wait(sm, &sm.o_done, (n - 1) & 1)) {
+                    if (!kSplit) {
+                        ok = false;
+                        break;
+                    }
+                    raise_abort<kSplit>(sm, p, peer);  // the loop stops at the next joint decision
+                }
                 tc_fence_after();
             }
             // tcgen05.ld/st are warp-collective: the whole warp takes the rescale
@@ -384,6 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.p_ready);
+        }
+        if (kSplit) {
+            if (threadIdx.x == 0 && armed > received) mbar_wait(&sm.rx_full, armed & 1);  // no copy may land after exit
+            ok = ok && !*(volatile int *)&sm.abort;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
         }
         if (!ok) raise_abort<kSplit>(sm, p, peer);
 
