@@ -13,16 +13,25 @@
 // The fp32 accumulator of 128 rows x 512 latent columns would fill all of an
 // SM's tensor memory, so when d_c > 256 a cluster of two CTAs shares the work
 // item: CTA 0 owns latent columns [0, 256), CTA 1 owns [256, d_c) plus the RoPE
-// key.  Each CTA loads only its own channel slice of every tile, computes the
-// partial score over that slice, and the pair swaps partial scores through
-// distributed shared memory; both then run the identical softmax (same sums in
-// the same order, so the same P) and each accumulates its half of O.
+// key.  Each CTA loads only its own channel slice of every tile and computes
+// the partial score over that slice; the pair swaps partial scores (rounded to
+// fp16 on both sides, so both CTAs add the same two numbers and derive the
+// same P) with one bulk shared-memory copy per tile and direction.  The swap of
+// tile n+1 is in flight while tile n's softmax runs.  Each CTA then
+// accumulates its half of O.  A CTA ships tile n+1 only after it has received
+// the peer's tile n, so the peer can be at most one tile ahead; with three
+// receive buffers a buffer is never refilled before it has been read, and no
+// "buffer free" signal has to cross the cluster.
 //
 // Tensor memory (512 columns): O [0, 256), S [256, 320), P (bf16) [320, 352),
-// Q slice (bf16, MMA A operand) [352, 512).
-// Warps: 0-3 softmax / epilogue (thread = row = TMEM lane), 4 TMA producer,
-// 5 TMEM owner + MMA issuer.  Every wait is bounded; a lost wait records
-// MLA_ERR_TIMEOUT, drains what is in flight, and the CTA returns.
+// Q slice (bf16, the A operand of the score MMA) [352, 512).
+// Warps 0-7: softmax and epilogue, two warps per TMEM lane quadrant (warp w
+// owns rows 32*(w%4) .. +31 and token columns 32*(w/4) .. +31 of each tile);
+// warp 8: TMA producer; warp 9: TMEM owner and MMA issuer.  Every wait is
+// bounded; a lost wait records MLA_ERR_TIMEOUT, drains what is in flight, and
+// the CTA returns.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "sm100.cuh"
@@ -35,14 +44,24 @@ using namespace sm100;
 
 constexpr int kRows = 128;        // query rows per work item (MMA M)
 constexpr int kTile = 64;         // tokens per tile (MMA N of the score, K of the sum)
+constexpr int kHalf = kTile / 2;  // tokens per softmax thread
 constexpr int kStages = 4;        // tiles in flight
+constexpr int kPrefetch = 8;      // tiles prefetched into L2 ahead of their shared-memory load
 constexpr int kMaxBoxes = 5;      // 64-channel boxes per tile and CTA (320 channels)
 constexpr int kBoxBytes = kTile * 128;
 constexpr int kStageBytes = kMaxBoxes * kBoxBytes;  // 40 KB
-constexpr int kXBytes = kRows * kTile * 4;  // one partial-score tile, fp32 (32 KB)
-constexpr int kThreads = 192;
+constexpr int kXBytes = kRows * kTile * 2;          // one partial-score tile in fp16 (16 KB)
+constexpr int kRxBufs = 3;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
+constexpr float kF16Max = 65504.f;
+
+// named barriers (0 is __syncthreads)
+constexpr uint32_t kBarSoftmax = 1;   // the 256 softmax threads
+constexpr uint32_t kBarPairBase = 2;  // + quadrant: the two warps sharing a quadrant (64 threads)
 
 struct Geo {
     int k0;      // first channel of this CTA's contraction slice (= first latent column of its O slice)
@@ -54,15 +73,19 @@ struct Geo {
 struct Smem {
     uint8_t kv[kStages][kStageBytes];
     // split mode: this CTA's partial scores staged for the bulk copy to the peer,
-    // and the peer's partial scores received.  Row r's 16-byte chunk c sits at
-    // chunk c ^ (r % 16), so that a warp's row-per-thread accesses do not collide.
-    float tx[kRows * kTile];
-    float rx[kRows * kTile];
+    // and the peer's partial scores received (tile u in buffer u % 3).  Row r is
+    // 128 B (64 fp16); its 16-byte chunk c sits at chunk c ^ (r % 8).
+    __half tx[kRows * kTile];
+    __half rx[kRxBufs][kRows * kTile];
+    // per half-row values the two warps of a quadrant exchange: tile maxima in
+    // the loop, softmax sums in the epilogue
+    float pair[2][kRows];
     uint64_t full[kStages], empty[kStages];
-    uint64_t q_ready, s_full, s_free, p_ready, o_done, rx_full, peer_rx_free, drain;
+    uint64_t q_ready, s_full, s_free, p_ready, o_done, drain;
+    uint64_t rx_full[kRxBufs];
     uint32_t tmem_base;
     int abort;  // set by this CTA or, remotely, by the peer
-    int stop;   // the softmax warps' common decision to leave the tile loop
+    int stop[2];  // the softmax warps' joint decision to leave the tile loop, by tile parity
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -104,6 +127,31 @@ __device__ __forceinline__ void raise_abort(Smem &sm, const AttnParams &p, uint3
     }
 }
 
+// This thread's 32 partial scores of the tile in S (tensor memory).
+__device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[kHalf]) {
+    uint32_t u0[16], u1[16];
+    tmem_ld16(taddr, u0);
+    tmem_ld16(taddr + 16, u1);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        s[e] = __uint_as_float(u0[e]);
+        s[16 + e] = __uint_as_float(u1[e]);
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    lo = fminf(fmaxf(lo, -kF16Max), kF16Max);
+    hi = fminf(fmaxf(hi, -kF16Max), kF16Max);
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2 *>(&u);
+    return __half22float2(h);
+}
+
 template <bool kSplit, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc(const __grid_constant__ CUtensorMap tm_kv, const AttnParams p, const Geo g0, const Geo g1) {
@@ -129,30 +177,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], 1);
         }
-        mbar_init(&sm.q_ready, 128);
+        mbar_init(&sm.q_ready, kSoftmaxThreads);
         mbar_init(&sm.s_full, 1);
-        mbar_init(&sm.s_free, 128);
-        mbar_init(&sm.p_ready, 128);
+        mbar_init(&sm.s_free, kSoftmaxThreads);
+        mbar_init(&sm.p_ready, kSoftmaxThreads);
         mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.rx_full, 1);
-        mbar_init(&sm.peer_rx_free, 1);
         mbar_init(&sm.drain, 1);
+        for (int i = 0; i < kRxBufs; ++i) mbar_init(&sm.rx_full[i], 1);
         sm.abort = 0;
-        sm.stop = 0;
+        sm.stop[0] = sm.stop[1] = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tm_kv);
     }
     if (!seq_ok && split == 0 && rb == 0 && rank == 0 && threadIdx.x == 0) set_status(p.status, MLA_ERR_SEQLEN);
-    if (warp == 5) tmem_alloc<512>(&sm.tmem_base);
+    if (warp == kMmaWarp) tmem_alloc<512>(&sm.tmem_base);
     tc_fence_before();
     if (kSplit) cluster_sync();
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == 4) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
+        // Tiles are prefetched into L2 kPrefetch tiles ahead of their shared-memory
+        // load, so the DRAM latency overlaps without holding shared memory.
         if (lane == 0) {
+            // y / z coordinates of tile n's box, or false if its page is outside the pool
+            auto coords = [&](int n, int &y, int &z) -> bool {
+                const int tok = t0 + n * kTile;
+                if (kPaged) {
+                    const int page = __ldg(p.block_table + (long long)b * p.max_pages + tok / p.page_size);
+                    y = page * p.page_size + tok % p.page_size;
+                    z = 0;
+                    return page >= 0 && page < p.num_pages;
+                }
+                y = tok;
+                z = b;
+                return true;
+            };
+            auto prefetch = [&](int n) {
+                int y, z;
+                if (n >= ntiles || !coords(n, y, z)) return;
+                for (int bx = 0; bx < g.nbox; ++bx) {
+                    if (kPaged) tma_prefetch_2d(&tm_kv, g.k0 + 64 * bx, y);
+                    else tma_prefetch_3d(&tm_kv, g.k0 + 64 * bx, y, z);
+                }
+            };
+            for (int n = 0; n < kPrefetch; ++n) prefetch(n);
             int issued = 0;
             for (int n = 0; n < ntiles; ++n) {
                 const int s = n % kStages;
@@ -160,95 +231,100 @@ __global__ void __launch_bounds__(kThreads, 1)
                     raise_abort<kSplit>(sm, p, peer);
                     break;
                 }
-                const int tok = t0 + n * kTile;
-                int x0 = g.k0, y = 0, z = 0;
-                if (kPaged) {
-                    int page = __ldg(p.block_table + (long long)b * p.max_pages + tok / p.page_size);
-                    if (page < 0 || page >= p.num_pages) {
-                        set_status(p.status, MLA_ERR_PAGE);
-                        page = p.num_pages;  // wholly out of range: the box reads as zeros
-                    }
-                    y = page * p.page_size + tok % p.page_size;
-                } else {
-                    y = tok;
-                    z = b;
+                prefetch(n + kPrefetch);
+                int y, z;
+                if (!coords(n, y, z)) {
+                    set_status(p.status, MLA_ERR_PAGE);
+                    y = p.num_pages * p.page_size;  // wholly out of range: the box reads as zeros
                 }
                 mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
                 for (int bx = 0; bx < g.nbox; ++bx) {
-                    if (kPaged) tma_load_2d(sm.kv[s] + bx * kBoxBytes, &tm_kv, &sm.full[s], x0 + 64 * bx, y);
-                    else tma_load_3d(sm.kv[s] + bx * kBoxBytes, &tm_kv, &sm.full[s], x0 + 64 * bx, y, z);
+                    if (kPaged) tma_load_2d(sm.kv[s] + bx * kBoxBytes, &tm_kv, &sm.full[s], g.k0 + 64 * bx, y);
+                    else tma_load_3d(sm.kv[s] + bx * kBoxBytes, &tm_kv, &sm.full[s], g.k0 + 64 * bx, y, z);
                 }
                 issued = n + 1;
             }
-            // drain: every issued copy must land before this CTA may exit
+            // every issued copy must land before this CTA may exit
             const int first = issued > kStages ? issued - kStages : 0;
             for (int n = first; n < issued; ++n) mbar_wait(&sm.full[n % kStages], (n / kStages) & 1);
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
+        // Two independent streams of work share the tensor pipe: the score of tile
+        // k (needs tile k loaded and S(k-1) read by the softmax) and the sum of tile
+        // k (needs P(k)).  Whichever is ready is issued (sums first), so the score
+        // of the next tile runs under the softmax of the current one.
         const uint32_t idesc_qk = idesc_bf16(kRows, kTile, false, false);
         const uint32_t idesc_pv = idesc_bf16(kRows, g.vn, false, true);
         bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
-        for (int n = 0; n < ntiles && ok; ++n) {
-            const int s = n % kStages;
-            if (!warp_wait(sm, &sm.full[s], (n / kStages) & 1)) { ok = false; break; }
-            // tokens at or past the sequence end may hold anything (even NaN): zero
-            // them so that 0-weight products stay 0
-            const int tok = t0 + n * kTile;
-            const int valid = min(kTile, L - tok);
-            if (valid < kTile) {
-                for (int e = lane; e < (kTile - valid) * 8 * g.nbox; e += 32) {
-                    const int bx = e / ((kTile - valid) * 8);
-                    const int rr = valid + (e / 8) % (kTile - valid);
-                    reinterpret_cast<uint4 *>(sm.kv[s] + bx * kBoxBytes + rr * 128)[e % 8] = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (n >= 1 && !warp_wait(sm, &sm.s_free, (n - 1) & 1)) { ok = false; break; }
-            tc_fence_after();
+        int qk = 0, pv = 0;
+        uint64_t t_last = globaltimer_ns();
+        long long c_last = clock64();
+        while (ok && pv < ntiles) {
+            int action = 0;
             if (lane == 0) {
-                const uint32_t kvs = smem_u32(sm.kv[s]);
-                for (int ks = 0; ks < g.kw / 16; ++ks) {
-                    const uint64_t db = smem_desc_sw128(kvs + (ks / 4) * kBoxBytes + (ks % 4) * 32, 16, 1024);
-                    mma_ts(tmem + kColS, tmem + kColQ + ks * 8, db, idesc_qk, ks > 0);
-                }
-                mma_commit(&sm.s_full);
+                // the sum of tile pv gates the softmax of tile pv+1; the score of the
+                // tile after next is not needed before that, so the sum goes first
+                if (pv < qk && mbar_test_wait(&sm.p_ready, pv & 1))
+                    action = 2;
+                else if (qk < ntiles && mbar_test_wait(&sm.full[qk % kStages], (qk / kStages) & 1) &&
+                         (qk == 0 || mbar_test_wait(&sm.s_free, (qk - 1) & 1)))
+                    action = 1;
+                else if (*(volatile int *)&sm.abort || wait_expired(t_last, c_last))
+                    action = 3;
             }
-            __syncwarp();
-            if (n >= 1) {
-                if (!warp_wait(sm, &sm.p_ready, (n - 1) & 1)) { ok = false; break; }
+            action = __shfl_sync(0xffffffffu, action, 0);
+            if (action == 0) {
+                __nanosleep(20);  // leave the issue slots to the softmax warps of this sub-partition
+                continue;
+            }
+            if (action == 3) {
+                ok = false;
+                break;
+            }
+            if (action == 1) {
+                const int s = qk % kStages;
+                // tokens at or past the sequence end may hold anything (even NaN):
+                // zero them so that 0-weight products stay 0
+                const int tok = t0 + qk * kTile;
+                const int valid = min(kTile, L - tok);
+                if (valid < kTile) {
+                    for (int e = lane; e < (kTile - valid) * 8 * g.nbox; e += 32) {
+                        const int bx = e / ((kTile - valid) * 8);
+                        const int rr = valid + (e / 8) % (kTile - valid);
+                        reinterpret_cast<uint4 *>(sm.kv[s] + bx * kBoxBytes + rr * 128)[e % 8] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 tc_fence_after();
                 if (lane == 0) {
-                    const int sp = (n - 1) % kStages;
-                    const uint32_t kvs = smem_u32(sm.kv[sp]);
-                    for (int kt = 0; kt < kTile / 16; ++kt) {
-                        const uint64_t db = smem_desc_sw128(kvs + kt * 16 * 128, kBoxBytes, 1024);
-                        mma_ts(tmem + kColO, tmem + kColP + kt * 8, db, idesc_pv, (n - 1 > 0) || kt > 0);
+                    const uint32_t kvs = smem_u32(sm.kv[s]);
+                    for (int ks = 0; ks < g.kw / 16; ++ks) {
+                        const uint64_t db = smem_desc_sw128(kvs + (ks / 4) * kBoxBytes + (ks % 4) * 32, 16, 1024);
+                        mma_ts(tmem + kColS, tmem + kColQ + ks * 8, db, idesc_qk, ks > 0);
                     }
-                    mma_commit(&sm.o_done);
-                    mma_commit(&sm.empty[sp]);
+                    mma_commit(&sm.s_full);
                 }
-                __syncwarp();
-            }
-        }
-        if (ok && ntiles > 0) {
-            if (!warp_wait(sm, &sm.p_ready, (ntiles - 1) & 1)) {
-                ok = false;
+                ++qk;
             } else {
                 tc_fence_after();
-                if (lane == 0) {
-                    const int sp = (ntiles - 1) % kStages;
+                if (lane == 0) {  // O += P(pv) . V(pv), then release the tile's stage
+                    const int sp = pv % kStages;
                     const uint32_t kvs = smem_u32(sm.kv[sp]);
+#pragma unroll
                     for (int kt = 0; kt < kTile / 16; ++kt) {
                         const uint64_t db = smem_desc_sw128(kvs + kt * 16 * 128, kBoxBytes, 1024);
-                        mma_ts(tmem + kColO, tmem + kColP + kt * 8, db, idesc_pv, (ntiles - 1 > 0) || kt > 0);
+                        mma_ts(tmem + kColO, tmem + kColP + kt * 8, db, idesc_pv, (pv > 0) || kt > 0);
                     }
                     mma_commit(&sm.o_done);
                     mma_commit(&sm.empty[sp]);
                 }
-                __syncwarp();
+                ++pv;
             }
+            __syncwarp();
+            t_last = globaltimer_ns();
+            c_last = clock64();
         }
         if (!ok) raise_abort<kSplit>(sm, p, peer);
         // every MMA issued above must finish before tensor memory is released
@@ -257,20 +333,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&sm.drain, 0);  // time-bounded only: in-flight MMAs must land
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ softmax + epilogue (rows)
-        const int r = threadIdx.x;  // 0..127 == TMEM lane
+        // ------------------------------------------------------------ softmax + epilogue
+        const int quad = warp & 3, hf = warp >> 2;
+        const int r = quad * 32 + lane;  // this thread's row == TMEM lane
         const int gr = rb * kRows + r;
         const bool row_ok = seq_ok && gr < rows_total;
         const int qi = row_ok ? gr / p.H : 0;
         const int lim = L - p.s_q + qi;  // last visible token of this row
-        const uint32_t lane_base = tmem_lane_base(warp);
+        const uint32_t lane_base = tmem_lane_base(quad);
         const float scale_log2 = p.scale * 1.4426950408889634f;
         const int W = p.d_c + p.d_rope;
+        const uint32_t pair_bar = kBarPairBase + quad;
 
-        // Q slice -> TMEM (bf16 pairs), zero for padding rows / channels
+        // Q slice -> TMEM (bf16 pairs); the two warps of a quadrant take alternate
+        // 32-channel chunks; padding rows and channels are zero
         {
             const __nv_bfloat16 *qrow = p.q_cat + ((long long)b * rows_total + gr) * W;
-            for (int c0 = 0; c0 < g.kw; c0 += 32) {
+            for (int c0 = 32 * hf; c0 < g.kw; c0 += 64) {
                 uint32_t v[16];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -286,91 +365,103 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&sm.q_ready);
         }
 
-        uint32_t rx_peer = 0, rxfull_peer = 0, rxfree_peer = 0;
+        // the peer's first receive buffer and its barrier (the others are fixed strides away)
+        uint32_t rx_peer0 = 0, rxfull_peer0 = 0;
         if (kSplit) {
-            rx_peer = map_to_rank(smem_u32(sm.rx), peer);
-            rxfull_peer = map_to_rank(smem_u32(&sm.rx_full), peer);
-            rxfree_peer = map_to_rank(smem_u32(&sm.peer_rx_free), peer);
+            rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
+            rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
         }
-        const int sw = r & 15;  // chunk swizzle of this row in tx / rx
+        constexpr uint32_t kRxStride = sizeof(sm.rx[0]), kBarStride = sizeof(uint64_t);
+        const int sw = r & 7;  // chunk swizzle of this row in tx / rx
+        const uint32_t s_addr = tmem + lane_base + kColS + kHalf * hf;
 
-        float m2 = -INFINITY;  // running (possibly stale) maximum, log2 units
-        float l = 0.f;
-        bool ok = true;
-        int armed = -1, received = -1;  // last receive this CTA armed / completed (split mode)
-        for (int n = 0; n < ntiles; ++n) {
-            bool good = warp_wait(sm, &sm.s_full, n & 1);
-            tc_fence_after();
-            float s[kTile];
-            {
-                uint32_t u0[16], u1[16], u2[16], u3[16];
-                tmem_ld16(tmem + lane_base + kColS + 0, u0);
-                tmem_ld16(tmem + lane_base + kColS + 16, u1);
-                tmem_ld16(tmem + lane_base + kColS + 32, u2);
-                tmem_ld16(tmem + lane_base + kColS + 48, u3);
-                tmem_ld_wait();
+        // Split mode: round this thread's partial scores to fp16 (in place, so both
+        // CTAs later add the same values), stage them, and let thread 0 ship the
+        // tile to the peer once all 256 threads have staged.
+        auto send = [&](int u, float (&sp)[kHalf]) {
+            uint4 *txrow = reinterpret_cast<uint4 *>(sm.tx + r * kTile);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    s[e] = __uint_as_float(u0[e]);
-                    s[16 + e] = __uint_as_float(u1[e]);
-                    s[32 + e] = __uint_as_float(u2[e]);
-                    s[48 + e] = __uint_as_float(u3[e]);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = c * 8 + e * 2;
+                    w4[e] = pack_f16x2(sp[j], sp[j + 1]);
+                    const float2 back = unpack_f16x2(w4[e]);
+                    sp[j] = back.x;
+                    sp[j + 1] = back.y;
+                }
+                txrow[(4 * hf + c) ^ sw] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            fence_proxy_async_smem();
+            named_bar(kBarSoftmax, kSoftmaxThreads);
+            if (threadIdx.x == 0) {
+                const int buf = u % kRxBufs;
+                mbar_arrive_expect_tx(&sm.rx_full[buf], kXBytes);  // arm this CTA's receive of tile u
+                if (!*(volatile int *)&sm.abort) {
+                    bulk_copy_to_peer(rx_peer0 + buf * kRxStride, sm.tx, kXBytes, rxfull_peer0 + buf * kBarStride);
+                    bulk_commit();
                 }
             }
+        };
+
+        float m2 = -INFINITY;  // running (possibly stale) row maximum, log2 units (same in both halves)
+        float l = 0.f;         // this half-row's sum of weights
+        bool ok = true;
+        int armed = -1, received = -1;  // last receive armed / completed (thread 0, split mode)
+        float sc[kHalf];  // this thread's partial (split) or full scores of the current tile
+        if (ntiles > 0) {
+            if (!warp_wait(sm, &sm.s_full, 0)) raise_abort<kSplit>(sm, p, peer);
+            tc_fence_after();
+            load_scores(s_addr, sc);
             tc_fence_before();
             mbar_arrive(&sm.s_free);
             if (kSplit) {
-                // Swap partial scores with the peer: stage locally, one bulk copy
-                // each way (completing bytes on the receiver's barrier), sum.
-                // Named barriers keep the 128 threads in step; nobody leaves the loop
-                // between them, and the decision to stop is taken jointly.
-                float4 *txrow = reinterpret_cast<float4 *>(sm.tx + r * kTile);
-#pragma unroll
-                for (int c = 0; c < kTile / 4; ++c)
-                    txrow[c ^ sw] = make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
-                fence_proxy_async_smem();
-                named_bar(1, 128);
+                send(0, sc);
                 if (threadIdx.x == 0) {
-                    bool go = !*(volatile int *)&sm.abort;
-                    if (go && n >= 1 && !wait_bar<true>(sm, &sm.peer_rx_free, (n - 1) & 1)) {
-                        raise_abort<kSplit>(sm, p, peer);
-                        go = false;
-                    }
-                    mbar_arrive_expect_tx(&sm.rx_full, kXBytes);  // arm this CTA's receive of tile n
-                    armed = n;
-                    if (go) {
-                        bulk_copy_to_peer(rx_peer, sm.tx, kXBytes, rxfull_peer);
-                        bulk_commit();
-                    }
+                    armed = 0;
+                    bulk_wait_read_all();  // tx is restaged for tile 1 below
                 }
-                if (warp_wait<true>(sm, &sm.rx_full, n & 1)) {
+                named_bar(kBarSoftmax, kSoftmaxThreads);
+            }
+        }
+        for (int n = 0; n < ntiles; ++n) {
+            // next tile's scores (the MMA computes S(n+1) as soon as S(n) was read)
+            float sn[kHalf];
+            const bool more = n + 1 < ntiles;
+            if (more) {
+                if (!warp_wait(sm, &sm.s_full, (n + 1) & 1)) raise_abort<kSplit>(sm, p, peer);
+                tc_fence_after();
+                load_scores(s_addr, sn);
+                tc_fence_before();
+                mbar_arrive(&sm.s_free);
+            }
+            if (kSplit) {
+                // the peer's partial of tile n has to be here before tile n+1 is shipped
+                const int buf = n % kRxBufs;
+                if (warp_wait<true>(sm, &sm.rx_full[buf], (n / kRxBufs) & 1)) {
                     if (threadIdx.x == 0) received = n;
                 } else {
-                    good = false;
+                    raise_abort<kSplit>(sm, p, peer);
                 }
-                const float4 *rxrow = reinterpret_cast<const float4 *>(sm.rx + r * kTile);
+                if (more) {
+                    send(n + 1, sn);
+                    if (threadIdx.x == 0) armed = n + 1;
+                }
+                const uint4 *rxrow = reinterpret_cast<const uint4 *>(sm.rx[buf] + r * kTile);
 #pragma unroll
-                for (int c = 0; c < kTile / 4; ++c) {
-                    const float4 v = rxrow[c ^ sw];
-                    s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v = rxrow[(4 * hf + c) ^ sw];
+                    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = unpack_f16x2(w4[e]);
+                        sc[c * 8 + e * 2] += f.x;
+                        sc[c * 8 + e * 2 + 1] += f.y;
+                    }
                 }
-                if (!good) raise_abort<kSplit>(sm, p, peer);
-                if (threadIdx.x == 0) {
-                    bulk_wait_read_all();  // tx may be rewritten next tile
-                    sm.stop = *(volatile int *)&sm.abort;
-                }
-                named_bar(1, 128);
-                const bool stop = *(volatile int *)&sm.stop;
-                if (threadIdx.x == 0 && !stop) mbar_arrive_remote(rxfree_peer);  // the peer may refill rx
-                if (stop) {
-                    ok = false;
-                    break;
-                }
-            } else if (!good) {
-                ok = false;
-                break;
             }
-            // scale, mask (only tiles that reach past a limit), tile maximum
+            // scale, mask (only tiles that reach past a limit), half-row maximum
             const int tok0 = t0 + n * kTile;
             bool tile_ok = true;
             if (kPaged) {
@@ -378,22 +469,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_ok = page >= 0 && page < p.num_pages;  // tokens of a bad page are skipped
             }
             const bool whole = tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q;
-            float tmax = -INFINITY;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
             if (whole) {
 #pragma unroll
-                for (int j = 0; j < kTile; ++j) {
-                    s[j] *= scale_log2;
-                    tmax = fmaxf(tmax, s[j]);
+                for (int j = 0; j < kHalf; j += 2) {
+                    sc[j] *= scale_log2;
+                    sc[j + 1] *= scale_log2;
+                    mx0 = fmaxf(mx0, sc[j]);
+                    mx1 = fmaxf(mx1, sc[j + 1]);
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < kTile; ++j) {
-                    const int tok = tok0 + j;
+                for (int j = 0; j < kHalf; ++j) {
+                    const int tok = tok0 + kHalf * hf + j;
                     const bool vis = tile_ok && row_ok && tok < t1 && tok <= lim;
-                    s[j] = vis ? s[j] * scale_log2 : -INFINITY;
-                    tmax = fmaxf(tmax, s[j]);
+                    sc[j] = vis ? sc[j] * scale_log2 : -INFINITY;
+                    mx0 = fmaxf(mx0, sc[j]);
                 }
             }
+            // the two halves of the row agree on the maximum
+            sm.pair[hf][r] = fmaxf(mx0, mx1);
+            named_bar(pair_bar, 64);
+            const float tmax = fmaxf(sm.pair[0][r], sm.pair[1][r]);
             float m_use = m2, alpha = 1.f;
             bool rescale = false;
             if (tmax > m2 + kRescaleLog2 || (m2 == -INFINITY && tmax > -INFINITY)) {
@@ -403,38 +500,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
             }
-            float sum = 0.f;
-            uint32_t pk[kTile / 2];
+            float sum0 = 0.f, sum1 = 0.f;
+            uint32_t pk[16];
             if (m_use == -INFINITY) {
 #pragma unroll
-                for (int j = 0; j < kTile / 2; ++j) pk[j] = 0u;
+                for (int j = 0; j < 16; ++j) pk[j] = 0u;
             } else {
 #pragma unroll
-                for (int j = 0; j < kTile; j += 2) {
-                    const float a = ex2(s[j] - m_use);
-                    const float c = ex2(s[j + 1] - m_use);
-                    sum += a + c;
+                for (int j = 0; j < kHalf; j += 2) {
+                    const float a = ex2(sc[j] - m_use);
+                    const float c = ex2(sc[j + 1] - m_use);
+                    sum0 += a;
+                    sum1 += c;
                     pk[j / 2] = pack_bf16x2(a, c);
                 }
             }
-            l = l * alpha + sum;
+            l = l * alpha + (sum0 + sum1);
             m2 = m_use;
             // the previous P . V must be done before O is rescaled or P overwritten
             if (n >= 1) {
-                if (!warp_wait(sm, &sm.o_done, (n - 1) & 1)) {
-                    if (!kSplit) {
-                        ok = false;
-                        break;
-                    }
-                    raise_abort<kSplit>(sm, p, peer);  // the loop stops at the next joint decision
-                }
+                if (!warp_wait(sm, &sm.o_done, (n - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
                 tc_fence_after();
             }
             // tcgen05.ld/st are warp-collective: the whole warp takes the rescale
-            // path if any of its rows needs it (alpha = 1 for the others)
+            // path if any of its rows needs it (alpha = 1 for the others); each warp
+            // of the quadrant rescales its half of O's columns
             if (n >= 1 && __any_sync(0xffffffffu, rescale)) {
                 if (!rescale) alpha = 1.f;
-                for (int c = 0; c < g.vn; c += 16) {
+                const int half_cols = g.vn / 2;
+                for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                     uint32_t u[16];
                     tmem_ld16(tmem + lane_base + kColO + c, u);
                     tmem_ld_wait();
@@ -443,23 +537,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st16(tmem + lane_base + kColO + c, u);
                 }
             }
-            {
-                uint32_t h0[16], h1[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) { h0[e] = pk[e]; h1[e] = pk[16 + e]; }
-                tmem_st16(tmem + lane_base + kColP, h0);
-                tmem_st16(tmem + lane_base + kColP + 16, h1);
-            }
+            tmem_st16(tmem + lane_base + kColP + 16 * hf, pk);
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.p_ready);
+
+            // joint decision point of the 256 softmax threads
+            if (kSplit && threadIdx.x == 0) bulk_wait_read_all();  // tx may be restaged next tile
+            if (threadIdx.x == 0) sm.stop[n & 1] = *(volatile int *)&sm.abort;
+            named_bar(kBarSoftmax, kSoftmaxThreads);
+            const bool stop = *(volatile int *)&sm.stop[n & 1];
+            if (stop) {
+                ok = false;
+                break;
+            }
+#pragma unroll
+            for (int j = 0; j < kHalf; ++j) sc[j] = sn[j];
         }
-        if (kSplit) {
-            if (threadIdx.x == 0 && armed > received) mbar_wait(&sm.rx_full, armed & 1);  // no copy may land after exit
-            ok = ok && !*(volatile int *)&sm.abort;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-        }
-        if (!ok) raise_abort<kSplit>(sm, p, peer);
+        if (kSplit && threadIdx.x == 0 && armed > received)
+            mbar_wait(&sm.rx_full[armed % kRxBufs], (armed / kRxBufs) & 1);  // no copy may land after exit
+        ok = __shfl_sync(0xffffffffu, ok, 0);
 
         // ------------------------------------------------------------ epilogue
         bool have_o = ok && ntiles > 0;
@@ -470,34 +567,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
         }
+        sm.pair[hf][r] = l;  // the loop's last read of sm.pair came before the joint barrier
+        named_bar(pair_bar, 64);
+        const float l_row = sm.pair[0][r] + sm.pair[1][r];
         // TMEM reads below are warp-collective, so every lane runs them; only the
         // stores are guarded by the row bound
         const bool store = gr < rows_total;
         const float ln2 = 0.6931471805599453f;
+        const int half_cols = g.vn / 2;
+        const bool any = have_o && l_row > 0.f;
         if (p.num_splits == 1) {
-            const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
+            const float inv = any ? 1.f / l_row : 0.f;
             __nv_bfloat16 *dst = p.o_lat + ((long long)b * rows_total + gr) * p.d_c + g.k0;
-            for (int c = 0; c < g.vn; c += 16) {
+            for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
                 tmem_ld16(tmem + lane_base + kColO + c, u);
                 tmem_ld_wait();
                 uint32_t o8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
-                    o8[e] = pack_bf16x2(inv == 0.f ? 0.f : __uint_as_float(u[2 * e]) * inv,
-                                        inv == 0.f ? 0.f : __uint_as_float(u[2 * e + 1]) * inv);
+                    o8[e] = pack_bf16x2(any ? __uint_as_float(u[2 * e]) * inv : 0.f,
+                                        any ? __uint_as_float(u[2 * e + 1]) * inv : 0.f);
                 if (store) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
                     d4[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
                     d4[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
                 }
             }
-            if (store && rank == 0)
-                p.lse[(long long)b * rows_total + gr] = (have_o && l > 0.f) ? (m2 + __log2f(l)) * ln2 : -INFINITY;
+            if (store && rank == 0 && hf == 0)
+                p.lse[(long long)b * rows_total + gr] = any ? (m2 + __log2f(l_row)) * ln2 : -INFINITY;
         } else {
             const long long prow = ((long long)b * p.num_splits + split) * rows_total + gr;
             float *dst = p.part_acc + prow * p.d_c + g.k0;
-            for (int c = 0; c < g.vn; c += 16) {
+            for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
                 tmem_ld16(tmem + lane_base + kColO + c, u);
                 tmem_ld_wait();
@@ -505,15 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 *d4 = reinterpret_cast<float4 *>(dst + c);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        d4[e] = have_o ? make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
-                                                     __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                        d4[e] = any ? make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                                                  __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            if (store && rank == 0) {
-                const bool any = have_o && l > 0.f;
+            if (store && rank == 0 && hf == 0) {
                 p.part_ml[prow * 2 + 0] = any ? m2 * ln2 : -INFINITY;
-                p.part_ml[prow * 2 + 1] = any ? l : 0.f;
+                p.part_ml[prow * 2 + 1] = any ? l_row : 0.f;
             }
         }
         tc_fence_before();
@@ -521,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     __syncthreads();
     if (kSplit) cluster_sync();  // the peer may still touch this CTA's shared memory until here
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_free<512>(tmem);
     }
