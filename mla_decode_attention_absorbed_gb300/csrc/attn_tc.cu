@@ -19,17 +19,17 @@
 // same P) with one bulk shared-memory copy per tile and direction.  The swap of
 // tile n+1 is in flight while tile n's softmax runs.  Each CTA then
 // accumulates its half of O.  A CTA ships tile n+1 only after it has received
-// the peer's tile n, so the peer can be at most one tile ahead; with three
-// receive buffers a buffer is never refilled before it has been read, and no
-// "buffer free" signal has to cross the cluster.
+// and consumed the peer's tile n, so with two receive buffers (by tile parity)
+// a buffer is never refilled before it has been read, and no "buffer free"
+// signal has to cross the cluster.
 //
 // Tensor memory (512 columns): O [0, 256), S [256, 320), P (bf16) [320, 352),
 // Q slice (bf16, the A operand of the score MMA) [352, 512).
 // Warps 0-7: softmax and epilogue, two warps per TMEM lane quadrant (warp w
 // owns rows 32*(w%4) .. +31 and token columns 32*(w/4) .. +31 of each tile);
-// warp 8: TMA producer; warp 9: TMEM owner and MMA issuer.  Every wait is
-// bounded; a lost wait records MLA_ERR_TIMEOUT, drains what is in flight, and
-// the CTA returns.
+// warp 8: TMA producer; warp 9: TMEM owner and MMA issuer; warp 10: ships the
+// staged partial scores to the peer.  Every wait is bounded; a lost wait
+// records MLA_ERR_TIMEOUT, drains what is in flight, and the CTA returns.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -46,22 +46,17 @@ constexpr int kRows = 128;        // query rows per work item (MMA M)
 constexpr int kTile = 64;         // tokens per tile (MMA N of the score, K of the sum)
 constexpr int kHalf = kTile / 2;  // tokens per softmax thread
 constexpr int kStages = 4;        // tiles in flight
-constexpr int kPrefetch = 8;      // tiles prefetched into L2 ahead of their shared-memory load
 constexpr int kMaxBoxes = 5;      // 64-channel boxes per tile and CTA (320 channels)
 constexpr int kBoxBytes = kTile * 128;
 constexpr int kStageBytes = kMaxBoxes * kBoxBytes;  // 40 KB
 constexpr int kXBytes = kRows * kTile * 2;          // one partial-score tile in fp16 (16 KB)
-constexpr int kRxBufs = 3;
 constexpr int kSoftmaxThreads = 256;
-constexpr int kThreads = kSoftmaxThreads + 64;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10;
+constexpr int kThreads = kSoftmaxThreads + 96;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
 constexpr float kF16Max = 65504.f;
-
-// named barriers (0 is __syncthreads)
-constexpr uint32_t kBarSoftmax = 1;   // the 256 softmax threads
-constexpr uint32_t kBarPairBase = 2;  // + quadrant: the two warps sharing a quadrant (64 threads)
+constexpr uint32_t kBarPairBase = 1;  // named barrier 1 + quadrant: the two warps of a quadrant (64 threads)
 
 struct Geo {
     int k0;      // first channel of this CTA's contraction slice (= first latent column of its O slice)
@@ -72,20 +67,22 @@ struct Geo {
 
 struct Smem {
     uint8_t kv[kStages][kStageBytes];
-    // split mode: this CTA's partial scores staged for the bulk copy to the peer,
-    // and the peer's partial scores received (tile u in buffer u % 3).  Row r is
-    // 128 B (64 fp16); its 16-byte chunk c sits at chunk c ^ (r % 8).
+    // split mode: this CTA's scaled partial scores (fp16) staged for the bulk copy
+    // to the peer, and the peer's received by tile parity.  Row r is 128 B (64
+    // fp16); its 16-byte chunk c sits at chunk c ^ (r % 8).
     __half tx[kRows * kTile];
-    __half rx[kRxBufs][kRows * kTile];
-    // per half-row values the two warps of a quadrant exchange: tile maxima in
-    // the loop, softmax sums in the epilogue
-    float pair[2][kRows];
+    __half rx[2][kRows * kTile];
+    // per half-row values the two warps of a quadrant exchange, by tile parity:
+    // tile maxima in the loop, softmax sums in the epilogue
+    float pair[2][2][kRows];
+    int pair_stop[4][2];  // each quadrant's joint decision to leave the tile loop, by tile parity
     uint64_t full[kStages], empty[kStages];
     uint64_t q_ready, s_full, s_free, p_ready, o_done, drain;
-    uint64_t rx_full[kRxBufs];
+    uint64_t staged, tx_free, rx_full[2];
     uint32_t tmem_base;
-    int abort;  // set by this CTA or, remotely, by the peer
-    int stop[2];  // the softmax warps' joint decision to leave the tile loop, by tile parity
+    int abort;    // set by this CTA or, remotely, by the peer
+    int armed;    // last tile whose receive the exchange warp armed
+    int received; // last tile the softmax warps received
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -127,7 +124,7 @@ __device__ __forceinline__ void raise_abort(Smem &sm, const AttnParams &p, uint3
     }
 }
 
-// This thread's 32 partial scores of the tile in S (tensor memory).
+// This thread's 32 scores of the tile in S (tensor memory).
 __device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[kHalf]) {
     uint32_t u0[16], u1[16];
     tmem_ld16(taddr, u0);
@@ -183,9 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.p_ready, kSoftmaxThreads);
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.drain, 1);
-        for (int i = 0; i < kRxBufs; ++i) mbar_init(&sm.rx_full[i], 1);
+        mbar_init(&sm.staged, kSoftmaxThreads);
+        mbar_init(&sm.tx_free, 1);
+        mbar_init(&sm.rx_full[0], 1);
+        mbar_init(&sm.rx_full[1], 1);
+        for (int q = 0; q < 4; ++q) sm.pair_stop[q][0] = sm.pair_stop[q][1] = 0;
         sm.abort = 0;
-        sm.stop[0] = sm.stop[1] = 0;
+        sm.armed = sm.received = -1;
         fence_mbar_init();
         tma_prefetch_desc(&tm_kv);
     }
@@ -199,8 +200,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
-        // Tiles are prefetched into L2 kPrefetch tiles ahead of their shared-memory
-        // load, so the DRAM latency overlaps without holding shared memory.
         if (lane == 0) {
             // y / z coordinates of tile n's box, or false if its page is outside the pool
             auto coords = [&](int n, int &y, int &z) -> bool {
@@ -215,15 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 z = b;
                 return true;
             };
-            auto prefetch = [&](int n) {
-                int y, z;
-                if (n >= ntiles || !coords(n, y, z)) return;
-                for (int bx = 0; bx < g.nbox; ++bx) {
-                    if (kPaged) tma_prefetch_2d(&tm_kv, g.k0 + 64 * bx, y);
-                    else tma_prefetch_3d(&tm_kv, g.k0 + 64 * bx, y, z);
-                }
-            };
-            for (int n = 0; n < kPrefetch; ++n) prefetch(n);
             int issued = 0;
             for (int n = 0; n < ntiles; ++n) {
                 const int s = n % kStages;
@@ -231,7 +221,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     raise_abort<kSplit>(sm, p, peer);
                     break;
                 }
-                prefetch(n + kPrefetch);
                 int y, z;
                 if (!coords(n, y, z)) {
                     set_status(p.status, MLA_ERR_PAGE);
@@ -256,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // of the next tile runs under the softmax of the current one.
         const uint32_t idesc_qk = idesc_bf16(kRows, kTile, false, false);
         const uint32_t idesc_pv = idesc_bf16(kRows, g.vn, false, true);
+        // descriptors of stage 0; a stage's are 16-byte-unit offsets of these
+        const uint64_t qk_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
+        const uint64_t pv_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), kBoxBytes, 1024);
+        const int nks = g.kw / 16;
         bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
         int qk = 0, pv = 0;
         uint64_t t_last = globaltimer_ns();
@@ -299,11 +292,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t kvs = smem_u32(sm.kv[s]);
-                    for (int ks = 0; ks < g.kw / 16; ++ks) {
-                        const uint64_t db = smem_desc_sw128(kvs + (ks / 4) * kBoxBytes + (ks % 4) * 32, 16, 1024);
-                        mma_ts(tmem + kColS, tmem + kColQ + ks * 8, db, idesc_qk, ks > 0);
-                    }
+                    // fully unrolled: each MMA is an immediate add to the descriptor and
+                    // the A address, so one thread keeps the tensor pipe fed
+                    const uint64_t db = qk_desc0 + (uint64_t)((s * kStageBytes) >> 4);
+                    const uint32_t d_s = tmem + kColS, a_q = tmem + kColQ;
+#pragma unroll
+                    for (int ks = 0; ks < kMaxBoxes * 4; ++ks)
+                        if (ks < nks)
+                            mma_ts(d_s, a_q + ks * 8, db + (uint64_t)(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4),
+                                   idesc_qk, ks > 0);
                     mma_commit(&sm.s_full);
                 }
                 ++qk;
@@ -311,12 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (lane == 0) {  // O += P(pv) . V(pv), then release the tile's stage
                     const int sp = pv % kStages;
-                    const uint32_t kvs = smem_u32(sm.kv[sp]);
+                    const uint64_t db = pv_desc0 + (uint64_t)((sp * kStageBytes) >> 4);
 #pragma unroll
-                    for (int kt = 0; kt < kTile / 16; ++kt) {
-                        const uint64_t db = smem_desc_sw128(kvs + kt * 16 * 128, kBoxBytes, 1024);
-                        mma_ts(tmem + kColO, tmem + kColP + kt * 8, db, idesc_pv, (pv > 0) || kt > 0);
-                    }
+                    for (int kt = 0; kt < kTile / 16; ++kt)
+                        mma_ts(tmem + kColO, tmem + kColP + kt * 8, db + (uint64_t)(kt * (16 * 128 / 16)), idesc_pv,
+                               (pv > 0) || kt > 0);
                     mma_commit(&sm.o_done);
                     mma_commit(&sm.empty[sp]);
                 }
@@ -332,6 +328,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         mbar_wait(&sm.drain, 0);  // time-bounded only: in-flight MMAs must land
         __syncwarp();
+    } else if (warp == kExchangeWarp) {
+        // ------------------------------------------------------------ score exchange (split mode)
+        // Ships each staged tile of partial scores to the peer with one bulk copy
+        // that completes on the peer's receive barrier, then frees the staging buffer.
+        if (kSplit && lane == 0) {
+            const uint32_t rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
+            const uint32_t rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
+            for (int u = 0; u < ntiles; ++u) {
+                if (!wait_bar(sm, &sm.staged, u & 1)) {
+                    raise_abort<kSplit>(sm, p, peer);
+                    break;
+                }
+                mbar_arrive_expect_tx(&sm.rx_full[u & 1], kXBytes);  // arm this CTA's receive of tile u
+                *(volatile int *)&sm.armed = u;
+                bulk_copy_to_peer(rx_peer0 + (u & 1) * (uint32_t)sizeof(sm.rx[0]), sm.tx, kXBytes,
+                                  rxfull_peer0 + (u & 1) * (uint32_t)sizeof(uint64_t));
+                bulk_commit();
+                bulk_wait_read_all();
+                mbar_arrive(&sm.tx_free);
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int quad = warp & 3, hf = warp >> 2;
@@ -365,64 +382,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(&sm.q_ready);
         }
 
-        // the peer's first receive buffer and its barrier (the others are fixed strides away)
-        uint32_t rx_peer0 = 0, rxfull_peer0 = 0;
-        if (kSplit) {
-            rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
-            rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
-        }
-        constexpr uint32_t kRxStride = sizeof(sm.rx[0]), kBarStride = sizeof(uint64_t);
         const int sw = r & 7;  // chunk swizzle of this row in tx / rx
         const uint32_t s_addr = tmem + lane_base + kColS + kHalf * hf;
 
-        // Split mode: round this thread's partial scores to fp16 (in place, so both
-        // CTAs later add the same values), stage them, and let thread 0 ship the
-        // tile to the peer once all 256 threads have staged.
-        auto send = [&](int u, float (&sp)[kHalf]) {
+        // Split mode: scale this thread's partial scores, round them to fp16 (kept
+        // in `own`, so both CTAs later add the same two numbers), stage them for the
+        // exchange warp and move on.
+        auto stage = [&](int u, const float (&sp)[kHalf], uint32_t (&own)[kHalf / 2]) {
+            if (u >= 1 && !warp_wait(sm, &sm.tx_free, (u - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
+#pragma unroll
+            for (int j = 0; j < kHalf / 2; ++j) own[j] = pack_f16x2(sp[2 * j] * scale_log2, sp[2 * j + 1] * scale_log2);
             uint4 *txrow = reinterpret_cast<uint4 *>(sm.tx + r * kTile);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = c * 8 + e * 2;
-                    w4[e] = pack_f16x2(sp[j], sp[j + 1]);
-                    const float2 back = unpack_f16x2(w4[e]);
-                    sp[j] = back.x;
-                    sp[j + 1] = back.y;
-                }
-                txrow[(4 * hf + c) ^ sw] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
+            for (int c = 0; c < 4; ++c)
+                txrow[(4 * hf + c) ^ sw] = make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
             fence_proxy_async_smem();
-            named_bar(kBarSoftmax, kSoftmaxThreads);
-            if (threadIdx.x == 0) {
-                const int buf = u % kRxBufs;
-                mbar_arrive_expect_tx(&sm.rx_full[buf], kXBytes);  // arm this CTA's receive of tile u
-                if (!*(volatile int *)&sm.abort) {
-                    bulk_copy_to_peer(rx_peer0 + buf * kRxStride, sm.tx, kXBytes, rxfull_peer0 + buf * kBarStride);
-                    bulk_commit();
-                }
-            }
+            mbar_arrive(&sm.staged);
         };
 
         float m2 = -INFINITY;  // running (possibly stale) row maximum, log2 units (same in both halves)
         float l = 0.f;         // this half-row's sum of weights
         bool ok = true;
-        int armed = -1, received = -1;  // last receive armed / completed (thread 0, split mode)
-        float sc[kHalf];  // this thread's partial (split) or full scores of the current tile
+        int last_bar = -1;       // last tile whose pair barrier this thread passed
+        uint32_t own[kHalf / 2];  // split: this CTA's scaled fp16 partial of the current tile
+        float sc[kHalf];          // non-split: scaled scores of the current tile
         if (ntiles > 0) {
+            float s0[kHalf];
             if (!warp_wait(sm, &sm.s_full, 0)) raise_abort<kSplit>(sm, p, peer);
             tc_fence_after();
-            load_scores(s_addr, sc);
+            load_scores(s_addr, s0);
             tc_fence_before();
             mbar_arrive(&sm.s_free);
             if (kSplit) {
-                send(0, sc);
-                if (threadIdx.x == 0) {
-                    armed = 0;
-                    bulk_wait_read_all();  // tx is restaged for tile 1 below
-                }
-                named_bar(kBarSoftmax, kSoftmaxThreads);
+                stage(0, s0, own);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kHalf; ++j) sc[j] = s0[j] * scale_log2;
             }
         }
         for (int n = 0; n < ntiles; ++n) {
@@ -436,32 +431,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(&sm.s_free);
             }
+            float x[kHalf];  // scaled scores of tile n
             if (kSplit) {
-                // the peer's partial of tile n has to be here before tile n+1 is shipped
-                const int buf = n % kRxBufs;
-                if (warp_wait<true>(sm, &sm.rx_full[buf], (n / kRxBufs) & 1)) {
-                    if (threadIdx.x == 0) received = n;
+                // the peer's partial of tile n; it is consumed before tile n+1 is staged,
+                // which is what lets two receive buffers suffice
+                if (warp_wait<true>(sm, &sm.rx_full[n & 1], (n >> 1) & 1)) {
+                    if (threadIdx.x == 0) *(volatile int *)&sm.received = n;
                 } else {
                     raise_abort<kSplit>(sm, p, peer);
                 }
-                if (more) {
-                    send(n + 1, sn);
-                    if (threadIdx.x == 0) armed = n + 1;
-                }
-                const uint4 *rxrow = reinterpret_cast<const uint4 *>(sm.rx[buf] + r * kTile);
+                const uint4 *rxrow = reinterpret_cast<const uint4 *>(sm.rx[n & 1] + r * kTile);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 v = rxrow[(4 * hf + c) ^ sw];
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 f = unpack_f16x2(w4[e]);
-                        sc[c * 8 + e * 2] += f.x;
-                        sc[c * 8 + e * 2 + 1] += f.y;
+                        const float2 mine = unpack_f16x2(own[4 * c + e]);
+                        const float2 theirs = unpack_f16x2(w4[e]);
+                        x[8 * c + 2 * e] = mine.x + theirs.x;
+                        x[8 * c + 2 * e + 1] = mine.y + theirs.y;
                     }
                 }
+                if (more) stage(n + 1, sn, own);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kHalf; ++j) {
+                    x[j] = sc[j];
+                    sc[j] = sn[j] * scale_log2;
+                }
             }
-            // scale, mask (only tiles that reach past a limit), half-row maximum
+            // mask (only tiles that reach past a limit) and half-row maximum
             const int tok0 = t0 + n * kTile;
             bool tile_ok = true;
             if (kPaged) {
@@ -473,24 +473,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (whole) {
 #pragma unroll
                 for (int j = 0; j < kHalf; j += 2) {
-                    sc[j] *= scale_log2;
-                    sc[j + 1] *= scale_log2;
-                    mx0 = fmaxf(mx0, sc[j]);
-                    mx1 = fmaxf(mx1, sc[j + 1]);
+                    mx0 = fmaxf(mx0, x[j]);
+                    mx1 = fmaxf(mx1, x[j + 1]);
                 }
             } else {
 #pragma unroll
                 for (int j = 0; j < kHalf; ++j) {
                     const int tok = tok0 + kHalf * hf + j;
                     const bool vis = tile_ok && row_ok && tok < t1 && tok <= lim;
-                    sc[j] = vis ? sc[j] * scale_log2 : -INFINITY;
-                    mx0 = fmaxf(mx0, sc[j]);
+                    x[j] = vis ? x[j] : -INFINITY;
+                    mx0 = fmaxf(mx0, x[j]);
                 }
             }
-            // the two halves of the row agree on the maximum
-            sm.pair[hf][r] = fmaxf(mx0, mx1);
+            // the two halves of the row agree on the maximum, and on whether to go on
+            sm.pair[n & 1][hf][r] = fmaxf(mx0, mx1);
+            if (hf == 0 && lane == 0) sm.pair_stop[quad][n & 1] = *(volatile int *)&sm.abort;
             named_bar(pair_bar, 64);
-            const float tmax = fmaxf(sm.pair[0][r], sm.pair[1][r]);
+            last_bar = n;
+            if (*(volatile int *)&sm.pair_stop[quad][n & 1]) {
+                ok = false;
+                break;
+            }
+            const float tmax = fmaxf(sm.pair[n & 1][0][r], sm.pair[n & 1][1][r]);
             float m_use = m2, alpha = 1.f;
             bool rescale = false;
             if (tmax > m2 + kRescaleLog2 || (m2 == -INFINITY && tmax > -INFINITY)) {
@@ -508,8 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
                 for (int j = 0; j < kHalf; j += 2) {
-                    const float a = ex2(sc[j] - m_use);
-                    const float c = ex2(sc[j + 1] - m_use);
+                    const float a = ex2(x[j] - m_use);
+                    const float c = ex2(x[j + 1] - m_use);
                     sum0 += a;
                     sum1 += c;
                     pk[j / 2] = pack_bf16x2(a, c);
@@ -541,21 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&sm.p_ready);
-
-            // joint decision point of the 256 softmax threads
-            if (kSplit && threadIdx.x == 0) bulk_wait_read_all();  // tx may be restaged next tile
-            if (threadIdx.x == 0) sm.stop[n & 1] = *(volatile int *)&sm.abort;
-            named_bar(kBarSoftmax, kSoftmaxThreads);
-            const bool stop = *(volatile int *)&sm.stop[n & 1];
-            if (stop) {
-                ok = false;
-                break;
-            }
-#pragma unroll
-            for (int j = 0; j < kHalf; ++j) sc[j] = sn[j];
         }
-        if (kSplit && threadIdx.x == 0 && armed > received)
-            mbar_wait(&sm.rx_full[armed % kRxBufs], (armed / kRxBufs) & 1);  // no copy may land after exit
         ok = __shfl_sync(0xffffffffu, ok, 0);
 
         // ------------------------------------------------------------ epilogue
@@ -567,9 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
         }
-        sm.pair[hf][r] = l;  // the loop's last read of sm.pair came before the joint barrier
+        // the slot of the parity after the last pair barrier is free for the sums
+        const int ls = (last_bar + 1) & 1;
+        sm.pair[ls][hf][r] = l;
         named_bar(pair_bar, 64);
-        const float l_row = sm.pair[0][r] + sm.pair[1][r];
+        const float l_row = sm.pair[ls][0][r] + sm.pair[ls][1][r];
         // TMEM reads below are warp-collective, so every lane runs them; only the
         // stores are guarded by the row bound
         const bool store = gr < rows_total;
@@ -621,6 +613,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    // no incoming copy may land in this CTA's shared memory after it exits
+    if (kSplit && threadIdx.x == 0) {
+        for (int u = *(volatile int *)&sm.received + 1; u <= *(volatile int *)&sm.armed; ++u)
+            mbar_wait(&sm.rx_full[u & 1], (u >> 1) & 1);
+    }
     if (kSplit) cluster_sync();  // the peer may still touch this CTA's shared memory until here
     if (warp == kMmaWarp) {
         tc_fence_after();
