@@ -60,10 +60,14 @@ int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
     long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
     long long tiles = (maxL + 63) / 64;
     long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
-    long long units = (long long)d->B * row_blocks;
+    long long units = (long long)d->B * row_blocks;  // work items before splitting
     if (units <= 0) return 1;
-    // Enough pieces to cover every SM pair once, each piece at least 8 tiles long.
-    long long want = (kNumSMs / 2 + units - 1) / units;
+    // One work item runs on a pair of SMs when d_c > 256, else on one SM.  Split
+    // the history only while the pieces still fit in one wave of the GPU (more
+    // pieces would add a partial wave and the cross-split merge), and keep every
+    // piece at least 8 tiles long.
+    const long long slots = d->d_c > 256 ? kNumSMs / 2 : kNumSMs;
+    long long want = slots / units;
     long long cap = tiles / 8;
     if (want > cap) want = cap;
     if (want < 1) want = 1;
