@@ -251,8 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nks = g.kw / 16;
         bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
         int qk = 0, pv = 0;
-        uint64_t t_last = globaltimer_ns();
-        long long c_last = clock64();
+        // the timers are read only while idle: the first idle poll after an issue
+        // starts the clock of the wait
+        bool fresh = true;
+        uint64_t t_last = 0;
+        long long c_last = 0;
         while (ok && pv < ntiles) {
             int action = 0;
             if (lane == 0) {
@@ -263,7 +266,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else if (qk < ntiles && mbar_test_wait(&sm.full[qk % kStages], (qk / kStages) & 1) &&
                          (qk == 0 || mbar_test_wait(&sm.s_free, (qk - 1) & 1)))
                     action = 1;
-                else if (*(volatile int *)&sm.abort || wait_expired(t_last, c_last))
+                else if (*(volatile int *)&sm.abort)
+                    action = 3;
+                else if (fresh) {
+                    t_last = globaltimer_ns();
+                    c_last = clock64();
+                    fresh = false;
+                } else if (wait_expired(t_last, c_last))
                     action = 3;
             }
             action = __shfl_sync(0xffffffffu, action, 0);
@@ -319,8 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++pv;
             }
             __syncwarp();
-            t_last = globaltimer_ns();
-            c_last = clock64();
+            fresh = true;
         }
         if (!ok) raise_abort<kSplit>(sm, p, peer);
         // every MMA issued above must finish before tensor memory is released
@@ -362,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int W = p.d_c + p.d_rope;
         const uint32_t pair_bar = kBarPairBase + quad;
 
-        // Q slice -> TMEM (bf16 pairs); the two warps of a quadrant take alternate
-        // 32-channel chunks; padding rows and channels are zero
+        // Q slice -> TMEM (bf16 pairs), pre-multiplied by scale * log2(e) so that the
+        // score MMAs produce exponents in log2 units directly; the two warps of a
+        // quadrant take alternate 32-channel chunks; padding rows and channels are zero
         {
             const __nv_bfloat16 *qrow = p.q_cat + ((long long)b * rows_total + gr) * W;
             for (int c0 = 32 * hf; c0 < g.kw; c0 += 64) {
@@ -373,7 +382,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint4 u = make_uint4(0, 0, 0, 0);
                     const int ch = g.k0 + c0 + e * 8;
                     if (row_ok && ch < W && c0 + e * 8 < g.kw) u = *reinterpret_cast<const uint4 *>(qrow + ch);
-                    v[e * 4 + 0] = u.x; v[e * 4 + 1] = u.y; v[e * 4 + 2] = u.z; v[e * 4 + 3] = u.w;
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[k]);
+                        const float2 f = __bfloat1622float2(h);
+                        v[e * 4 + k] = pack_bf16x2(f.x * scale_log2, f.y * scale_log2);
+                    }
                 }
                 tmem_st16(tmem + lane_base + kColQ + c0 / 2, v);
             }
@@ -385,13 +400,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sw = r & 7;  // chunk swizzle of this row in tx / rx
         const uint32_t s_addr = tmem + lane_base + kColS + kHalf * hf;
 
-        // Split mode: scale this thread's partial scores, round them to fp16 (kept
-        // in `own`, so both CTAs later add the same two numbers), stage them for the
-        // exchange warp and move on.
+        // Split mode: round this thread's partial scores to fp16 (kept in `own`, so
+        // both CTAs later add the same two numbers), stage them for the exchange
+        // warp and move on.
         auto stage = [&](int u, const float (&sp)[kHalf], uint32_t (&own)[kHalf / 2]) {
             if (u >= 1 && !warp_wait(sm, &sm.tx_free, (u - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
 #pragma unroll
-            for (int j = 0; j < kHalf / 2; ++j) own[j] = pack_f16x2(sp[2 * j] * scale_log2, sp[2 * j + 1] * scale_log2);
+            for (int j = 0; j < kHalf / 2; ++j) own[j] = pack_f16x2(sp[2 * j], sp[2 * j + 1]);
             uint4 *txrow = reinterpret_cast<uint4 *>(sm.tx + r * kTile);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -417,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stage(0, s0, own);
             } else {
 #pragma unroll
-                for (int j = 0; j < kHalf; ++j) sc[j] = s0[j] * scale_log2;
+                for (int j = 0; j < kHalf; ++j) sc[j] = s0[j];
             }
         }
         for (int n = 0; n < ntiles; ++n) {
@@ -458,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kHalf; ++j) {
                     x[j] = sc[j];
-                    sc[j] = sn[j] * scale_log2;
+                    sc[j] = sn[j];
                 }
             }
             // mask (only tiles that reach past a limit) and half-row maximum
