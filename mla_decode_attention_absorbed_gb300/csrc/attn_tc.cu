@@ -27,9 +27,10 @@
 // Q slice (bf16, the A operand of the score MMA) [352, 512).
 // Warps 0-7: softmax and epilogue, two warps per TMEM lane quadrant (warp w
 // owns rows 32*(w%4) .. +31 and token columns 32*(w/4) .. +31 of each tile);
-// warp 8: TMA producer; warp 9: TMEM owner and MMA issuer; warp 10: ships the
-// staged partial scores to the peer.  Every wait is bounded; a lost wait
-// records MLA_ERR_TIMEOUT, drains what is in flight, and the CTA returns.
+// warp 8: TMA producer; warp 9: TMEM owner, issues the score MMAs; warp 10:
+// ships the staged partial scores to the peer; warp 11: issues the sum MMAs.
+// Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT, drains what is in
+// flight, and the CTA returns.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -51,8 +52,8 @@ constexpr int kBoxBytes = kTile * 128;
 constexpr int kStageBytes = kMaxBoxes * kBoxBytes;  // 40 KB
 constexpr int kXBytes = kRows * kTile * 2;          // one partial-score tile in fp16 (16 KB)
 constexpr int kSoftmaxThreads = 256;
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10;
-constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10, kSumWarp = 11;
+constexpr int kThreads = kSoftmaxThreads + 128;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
 constexpr float kF16Max = 65504.f;
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.s_free, kSoftmaxThreads);
         mbar_init(&sm.p_ready, kSoftmaxThreads);
         mbar_init(&sm.o_done, 1);
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.drain, 2);  // one commit from each MMA issuer
         mbar_init(&sm.staged, kSoftmaxThreads);
         mbar_init(&sm.tx_free, 1);
         mbar_init(&sm.rx_full[0], 1);
@@ -237,12 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int first = issued > kStages ? issued - kStages : 0;
             for (int n = first; n < issued; ++n) mbar_wait(&sm.full[n % kStages], (n / kStages) & 1);
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issuer
-        // Two independent streams of work share the tensor pipe: the score of tile
-        // k (needs tile k loaded and S(k-1) read by the softmax) and the sum of tile
-        // k (needs P(k)).  Whichever is ready is issued (sums first), so the score
-        // of the next tile runs under the softmax of the current one.
+    } else if (warp == kMmaWarp || warp == kSumWarp) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two independent streams share the tensor pipe: the scores (warp 9: tile
+        // k needs tile k loaded and S(k-1) read by the softmax) and the sums (warp
+        // 11: tile k needs P(k)).  Each score MMA accumulates into the previous
+        // one's result and waits out its latency; with the sums issued from a
+        // warp of their own they run in those gaps instead of queueing behind the
+        // whole chain (an issuing thread's next shared-memory operation waits for
+        // its queued MMAs, so one thread cannot keep both streams in flight).
+        const bool scores = warp == kMmaWarp;
         const uint32_t idesc_qk = idesc_bf16(kRows, kTile, false, false);
         const uint32_t idesc_pv = idesc_bf16(kRows, g.vn, false, true);
         // descriptors of stage 0; a stage's are 16-byte-unit offsets of these
@@ -250,45 +255,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pv_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), kBoxBytes, 1024);
         const int nks = g.kw / 16;
         bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
-        int qk = 0, pv = 0;
-        // the timers are read only while idle: the first idle poll after an issue
-        // starts the clock of the wait
-        bool fresh = true;
-        uint64_t t_last = 0;
-        long long c_last = 0;
-        while (ok && pv < ntiles) {
-            int action = 0;
-            if (lane == 0) {
-                // the sum of tile pv gates the softmax of tile pv+1; the score of the
-                // tile after next is not needed before that, so the sum goes first
-                if (pv < qk && mbar_test_wait(&sm.p_ready, pv & 1))
-                    action = 2;
-                else if (qk < ntiles && mbar_test_wait(&sm.full[qk % kStages], (qk / kStages) & 1) &&
-                         (qk == 0 || mbar_test_wait(&sm.s_free, (qk - 1) & 1)))
-                    action = 1;
-                else if (*(volatile int *)&sm.abort)
-                    action = 3;
-                else if (fresh) {
-                    t_last = globaltimer_ns();
-                    c_last = clock64();
-                    fresh = false;
-                } else if (wait_expired(t_last, c_last))
-                    action = 3;
-            }
-            action = __shfl_sync(0xffffffffu, action, 0);
-            if (action == 0) {
-                __nanosleep(20);  // leave the issue slots to the softmax warps of this sub-partition
-                continue;
-            }
-            if (action == 3) {
-                ok = false;
-                break;
-            }
-            if (action == 1) {
-                const int s = qk % kStages;
+        for (int n = 0; ok && n < ntiles; ++n) {
+            const int s = n % kStages;
+            if (scores) {
+                if (!warp_wait(sm, &sm.full[s], (n / kStages) & 1) || (n > 0 && !warp_wait(sm, &sm.s_free, (n - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
                 // tokens at or past the sequence end may hold anything (even NaN):
                 // zero them so that 0-weight products stay 0
-                const int tok = t0 + qk * kTile;
+                const int tok = t0 + n * kTile;
                 const int valid = min(kTile, L - tok);
                 if (valid < kTile) {
                     for (int e = lane; e < (kTile - valid) * 8 * g.nbox; e += 32) {
@@ -302,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (lane == 0) {
                     // fully unrolled: each MMA is an immediate add to the descriptor and
-                    // the A address, so one thread keeps the tensor pipe fed
+                    // the A address
                     const uint64_t db = qk_desc0 + (uint64_t)((s * kStageBytes) >> 4);
                     const uint32_t d_s = tmem + kColS, a_q = tmem + kColQ;
 #pragma unroll
@@ -312,23 +288,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    idesc_qk, ks > 0);
                     mma_commit(&sm.s_full);
                 }
-                ++qk;
             } else {
+                if (!warp_wait(sm, &sm.p_ready, n & 1)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
-                if (lane == 0) {  // O += P(pv) . V(pv), then release the tile's stage
-                    const int sp = pv % kStages;
-                    const uint64_t db = pv_desc0 + (uint64_t)((sp * kStageBytes) >> 4);
+                if (lane == 0) {  // O += P(n) . V(n), then release the tile's stage
+                    const uint64_t db = pv_desc0 + (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
                     for (int kt = 0; kt < kTile / 16; ++kt)
                         mma_ts(tmem + kColO, tmem + kColP + kt * 8, db + (uint64_t)(kt * (16 * 128 / 16)), idesc_pv,
-                               (pv > 0) || kt > 0);
+                               (n > 0) || kt > 0);
                     mma_commit(&sm.o_done);
-                    mma_commit(&sm.empty[sp]);
+                    mma_commit(&sm.empty[s]);
                 }
-                ++pv;
             }
             __syncwarp();
-            fresh = true;
         }
         if (!ok) raise_abort<kSplit>(sm, p, peer);
         // every MMA issued above must finish before tensor memory is released
