@@ -78,7 +78,8 @@ int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
 size_t attn_workspace_bytes(const mla_dims *d, int splits) {
     if (splits <= 1) return kStatusBytes;
     size_t rows = (size_t)d->B * splits * d->s_q * d->H;
-    return kStatusBytes + round_up(rows * 2 * sizeof(float), 256) + rows * (size_t)d->d_c * sizeof(float);
+    // per row: (m, l) of each CTA half, then the fp32 accumulator
+    return kStatusBytes + round_up(rows * 4 * sizeof(float), 256) + rows * (size_t)d->d_c * sizeof(float);
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -170,7 +171,7 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
         size_t rows = (size_t)dims->B * splits * dims->s_q * dims->H;
         char *base = (char *)workspace + kStatusBytes;
         p.part_ml = (float *)base;
-        p.part_acc = (float *)(base + round_up(rows * 2 * sizeof(float), 256));
+        p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
     }
     cudaError_t e = mla::launch_attn_tc(p, st);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

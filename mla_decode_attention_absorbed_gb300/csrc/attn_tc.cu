@@ -14,11 +14,13 @@
 // SM's tensor memory, so when d_c > 256 a cluster of two CTAs shares the work
 // item: CTA 0 owns latent columns [0, 256), CTA 1 owns [256, d_c) plus the RoPE
 // key.  Each CTA loads only its own channel slice of every tile and computes
-// the partial score over that slice; the pair swaps partial scores (rounded to
-// fp16 on both sides, so both CTAs add the same two numbers and derive the
-// same P) with one bulk shared-memory copy per tile and direction.  The swap of
-// tile n+1 is in flight while tile n's softmax runs.  Each CTA then
-// accumulates its half of O.  A CTA ships tile n+1 only after it has received
+// the partial score over that slice; the pair swaps partial scores (sent as
+// fp16) with one bulk shared-memory copy per tile and direction, and each CTA
+// adds the peer's to its own fp32 partial.  The swap of tile n+1 is in flight
+// while tile n's softmax runs.  Each CTA then runs the softmax of all rows and
+// accumulates its half of O; its running (m, l) describe that half (the two
+// CTAs' scores differ only by the fp16 rounding of the other CTA's partial,
+// so split partials carry one (m, l) per CTA).  A CTA ships tile n+1 only after it has received
 // and consumed the peer's tile n, so with two receive buffers (by tile parity)
 // a buffer is never refilled before it has been read, and no "buffer free"
 // signal has to cross the cluster.
@@ -56,7 +58,6 @@ constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10, kSumWarp = 11
 constexpr int kThreads = kSoftmaxThreads + 128;
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
-constexpr float kF16Max = 65504.f;
 constexpr uint32_t kBarPairBase = 1;  // named barrier 1 + quadrant: the two warps of a quadrant (64 threads)
 
 struct Geo {
@@ -138,11 +139,12 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[kHalf]) {
     }
 }
 
+// Two scores to fp16 (lo in the low half), saturating at +-65504 instead of
+// overflowing to infinity.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    lo = fminf(fmaxf(lo, -kF16Max), kF16Max);
-    hi = fminf(fmaxf(hi, -kF16Max), kF16Max);
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t *>(&h);
+    uint32_t d;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
@@ -379,14 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Split mode: round this thread's partial scores to fp16 (kept in `own`, so
         // both CTAs later add the same two numbers), stage them for the exchange
         // warp and move on.
-        auto stage = [&](int u, const float (&sp)[kHalf], uint32_t (&own)[kHalf / 2]) {
+        auto stage = [&](int u, const float (&sp)[kHalf]) {
             if (u >= 1 && !warp_wait(sm, &sm.tx_free, (u - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
+            uint32_t h16[kHalf / 2];
 #pragma unroll
-            for (int j = 0; j < kHalf / 2; ++j) own[j] = pack_f16x2(sp[2 * j], sp[2 * j + 1]);
+            for (int j = 0; j < kHalf / 2; ++j) h16[j] = pack_f16x2(sp[2 * j], sp[2 * j + 1]);
             uint4 *txrow = reinterpret_cast<uint4 *>(sm.tx + r * kTile);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                txrow[(4 * hf + c) ^ sw] = make_uint4(own[4 * c], own[4 * c + 1], own[4 * c + 2], own[4 * c + 3]);
+                txrow[(4 * hf + c) ^ sw] = make_uint4(h16[4 * c], h16[4 * c + 1], h16[4 * c + 2], h16[4 * c + 3]);
             fence_proxy_async_smem();
             mbar_arrive(&sm.staged);
         };
@@ -395,8 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l = 0.f;         // this half-row's sum of weights
         bool ok = true;
         int last_bar = -1;       // last tile whose pair barrier this thread passed
-        uint32_t own[kHalf / 2];  // split: this CTA's scaled fp16 partial of the current tile
-        float sc[kHalf];          // non-split: scaled scores of the current tile
+        float sc[kHalf];  // this CTA's (split: partial) scores of the current tile
         if (ntiles > 0) {
             float s0[kHalf];
             if (!warp_wait(sm, &sm.s_full, 0)) raise_abort<kSplit>(sm, p, peer);
@@ -404,12 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             load_scores(s_addr, s0);
             tc_fence_before();
             mbar_arrive(&sm.s_free);
-            if (kSplit) {
-                stage(0, s0, own);
-            } else {
+            if (kSplit) stage(0, s0);
 #pragma unroll
-                for (int j = 0; j < kHalf; ++j) sc[j] = s0[j];
-            }
+            for (int j = 0; j < kHalf; ++j) sc[j] = s0[j];
         }
         for (int n = 0; n < ntiles; ++n) {
             // next tile's scores (the MMA computes S(n+1) as soon as S(n) was read)
@@ -438,20 +437,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 mine = unpack_f16x2(own[4 * c + e]);
                         const float2 theirs = unpack_f16x2(w4[e]);
-                        x[8 * c + 2 * e] = mine.x + theirs.x;
-                        x[8 * c + 2 * e + 1] = mine.y + theirs.y;
+                        x[8 * c + 2 * e] = sc[8 * c + 2 * e] + theirs.x;
+                        x[8 * c + 2 * e + 1] = sc[8 * c + 2 * e + 1] + theirs.y;
                     }
                 }
-                if (more) stage(n + 1, sn, own);
+                if (more) stage(n + 1, sn);
             } else {
 #pragma unroll
-                for (int j = 0; j < kHalf; ++j) {
-                    x[j] = sc[j];
-                    sc[j] = sn[j];
-                }
+                for (int j = 0; j < kHalf; ++j) x[j] = sc[j];
             }
+#pragma unroll
+            for (int j = 0; j < kHalf; ++j) sc[j] = sn[j];
             // mask (only tiles that reach past a limit) and half-row maximum
             const int tok0 = t0 + n * kTile;
             bool tile_ok = true;
@@ -595,9 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            if (store && rank == 0 && hf == 0) {
-                p.part_ml[prow * 2 + 0] = any ? m2 * ln2 : -INFINITY;
-                p.part_ml[prow * 2 + 1] = any ? l_row : 0.f;
+            if (store && hf == 0) {  // this CTA's (m, l): its half of the columns is relative to them
+                p.part_ml[(prow * 2 + rank) * 2 + 0] = any ? m2 * ln2 : -INFINITY;
+                p.part_ml[(prow * 2 + rank) * 2 + 1] = any ? l_row : 0.f;
             }
         }
         tc_fence_before();

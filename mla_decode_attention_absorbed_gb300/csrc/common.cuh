@@ -24,7 +24,7 @@ struct AttnParams {
     float *lse;                   // [B][s_q][H]
     int num_splits;
     float *part_acc;              // [B][splits][s_q*H][d_c] (num_splits > 1)
-    float *part_ml;               // [B][splits][s_q*H][2]   (m, l)
+    float *part_ml;               // [B][splits][s_q*H][2 CTA halves][2]   (m, l)
     int *status;                  // device status word
 };
 
