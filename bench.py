@@ -376,6 +376,157 @@ def main_ours(args):
     print(json.dumps(line))
 
 
+# ------------------------------------------------------------------------- other rows of the path
+D_MODEL = 7168  # DeepSeek-V3 hidden width (the down-projection's contraction)
+
+
+def _timed_steps(step, K, flush, stream, dev):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    for k in range(K):
+        if flush is not None:
+            flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def main_op(args):
+    """One JSON line for a non-headline row of the path, same contract as the decode line."""
+    rank, world, local = dist_env()
+    active = init_dist(world, args.backend)
+    cfg = CONFIGS[args.config]
+    from mla_decode_attention_absorbed_gb300 import mla
+    from mla_decode_attention_absorbed_gb300.workloads import make_append_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    mla.load()
+    c = cfg.with_(seed=replica_seed(cfg.seed, rank))
+    inp = make_inputs(c)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    prob = mla.Problem.of(c)
+    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    pk = peaks()
+    assert args.op == "append"
+    app = make_append_inputs(c, D_MODEL)
+    a = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in app.items()}
+    ws = mla.alloc_workspace(mla.cache_append_workspace_size(prob, D_MODEL), dev)
+    M = c.B * c.s_q
+    # algorithmic work: every W_DKV, x and k_rope byte read once, the new cache rows written once
+    bytes_ = (D_MODEL * c.d_c + M * D_MODEL + M * c.d_rope + M * c.W) * 2 + c.B * 4
+    flops = 2 * M * D_MODEL * c.d_c
+
+    def step():
+        mla.cache_append(prob, a["x"], a["w_dkv"], a["k_rope"], cache, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st = mla.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
+    # the step's launches (host-side argument checks and tensor-map encoding done
+    # once at capture) replayed as one CUDA graph: the device time of the op, not
+    # the Python call around it
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier(active)
+    step_ms = _timed_steps(graph.replay, args.steps, flush, stream, dev)
+    barrier(active)
+    clocks.stop()
+    ms = reduce_max(sum(step_ms) / len(step_ms), active, "cuda" if active and args.backend == "nccl" else "cpu")
+    achieved = bytes_ / (ms * 1e-3) / 1e9
+
+    # end to end: pinned x / k_rope in, the appended rows out, every step
+    h_x, h_kr = app["x"].pin_memory(), app["k_rope"].pin_memory()
+    lens = inp["seq_lens"].to(torch.long)
+    pos = lens.repeat_interleave(c.s_q) - c.s_q + torch.arange(c.s_q).repeat(c.B)
+    if inp["block_table"] is None:
+        flat = torch.arange(c.B).repeat_interleave(c.s_q) * inp["kv"].shape[1] + pos
+    else:
+        page = inp["block_table"].to(torch.long)[torch.arange(c.B).repeat_interleave(c.s_q), pos // c.page_size]
+        flat = page * c.page_size + pos % c.page_size
+    flat = flat.to(dev)
+    kv_rows = d["kv"].view(-1, c.W)
+    gather = lambda: kv_rows.index_select(0, flat)  # noqa: E731
+    h_rows = torch.empty(M, c.W, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    rows_dev = torch.empty(M, c.W, dtype=torch.bfloat16, device=dev)
+    for _ in range(e2e_steps):
+        a["x"].copy_(h_x, non_blocking=True)
+        a["k_rope"].copy_(h_kr, non_blocking=True)
+        graph.replay()
+        rows_dev.copy_(gather())
+        h_rows.copy_(rows_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active,
+                        "cuda" if active and args.backend == "nccl" else "cpu")
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        t = time.perf_counter()
+        oracle.down_proj(app["x"], app["w_dkv"])
+        t = time.perf_counter() - t
+        cpu = {"value": bytes_ / t / 1e9, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+               "sample": f"the whole step: {M} tokens x d_model {D_MODEL} x d_c {c.d_c} in fp64, {t:.2f} s"}
+    line = {
+        "metric": "MLA cache append (latent down-projection of the new tokens) GB/s",
+        "value": bytes_ * world / (ms * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) hidden states, N(0,1/d_model) W_DKV)",
+        "config": {"workload": f"append to {workload_name(c)}, d_model={D_MODEL}",
+                   "l2": "L2 flushed between steps (256 MB write)",
+                   "launch": "the step's kernels replayed as a CUDA graph",
+                   "parallelism": f"{world} independent replica(s)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                     "kernel": "mla_cache_append (split-K tcgen05 GEMM + scatter)",
+                     "peak_source": pk["source"] + " HBM copy",
+                     "roofline_time_us": bytes_ / (pk["hbm_gbs"] * 1e9) * 1e6, "kernel_us": ms * 1e3,
+                     "tflops": flops / (ms * 1e-3) / 1e12},
+        "cpu_baseline": cpu,
+        "e2e": {"value": bytes_ * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": (h_x.numel() + h_kr.numel()) * 2, "d2h_bytes_per_step": h_rows.numel() * 2,
+                "note": "pinned host x / k_rope in, the appended cache rows back, every step"},
+        "gpu_launches": 2 * args.steps,  # split-K GEMM + scatter (the accumulator memset is a driver op)
+        "clocks": clocks.summary(),
+        "step_ms_min": min(step_ms),
+        "step_ms_median": statistics.median(step_ms),
+    }
+    print(json.dumps(line))
+
+
 # ------------------------------------------------------------------------- reference arm
 def main_reference(args):
     rank, world, local = dist_env()
@@ -444,6 +595,9 @@ def parse(argv=None):
     ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode", choices=["decode", "append"],
+                    help="decode: the absorbed decode step (headline); append: the cache append "
+                         "(latent down-projection of the new tokens, d_model = 7168)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         a.warmup = 3
@@ -454,7 +608,9 @@ def parse(argv=None):
 
 if __name__ == "__main__":
     args = parse()
-    if args.impl == "reference":
+    if args.op != "decode":
+        main_op(args)
+    elif args.impl == "reference":
         main_reference(args)
     else:
         main_ours(args)

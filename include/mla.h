@@ -12,6 +12,8 @@
  *                    over a contiguous or paged latent cache, split along the
  *                    history and merged with a log-sum-exp combine
  *   mla_out_proj     out = o_lat . W_UV                               per head
+ *   mla_cache_append c_kv = x . W_DKV of the new tokens, written with their
+ *                    (already rotated) RoPE keys into the latent cache
  *   mla_naive_decode the decompress-then-attend form, a comparison point only
  *                    ("The MLA decode speedup hiding in your model card",
  *                    section "The naive form, written out")
@@ -147,6 +149,30 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
  * o_lat [B][s_q][H][d_c], w_uv [H][d_c][d_v], out [B][s_q][H][d_v]. */
 MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_uv,
                          void *out, void *stream);
+
+/* Bytes of workspace mla_cache_append needs: the status word (256 B) and the
+ * fp32 partial sums of the split down-projection (a few MB at DeepSeek-V3
+ * widths).  Returns 0 for invalid arguments. */
+MLA_API size_t mla_cache_append_workspace_size(const mla_dims *dims, int d_model);
+
+/* The step before attention: compress the new tokens' hidden states into
+ * latents and append them to the cache ("MLA, dim by dim", "MLA Decode": the
+ * current token's x . W_DKV, of 2*d*d_c FLOPs, is appended to the latent cache;
+ * "Why MLA and MTP Fight Each Other", 4.1: the history-independent part of a
+ * decode step):
+ *   c[b,i,:] = sum_k x[b,i,k] * W_DKV[k,:]     (fp32 accumulate, bf16 in the cache)
+ * and row L_b - s_q + i of sequence b (L_b = seq_lens[b], which already counts
+ * the s_q new tokens) becomes [c[b,i,:] | k_rope[b,i,:]].  x [B][s_q][d_model],
+ * w_dkv [d_model][d_c], k_rope [B][s_q][d_rope] (already rotated; the library
+ * does no rotation).  The cache is described as for mla_decode_attn and its kv
+ * buffer is WRITTEN (it must be writable device memory); only the new rows
+ * change.  d_model must be a multiple of 8.  A length outside [s_q, capacity]
+ * (MLA_ERR_SEQLEN) or a block-table entry outside the pool (MLA_ERR_PAGE) is
+ * recorded in the workspace's status word and that token's row is not
+ * written.  The weight is streamed once, split along d_model over the GPU. */
+MLA_API int mla_cache_append(const mla_dims *dims, int d_model, const void *x, const void *w_dkv,
+                             const void *k_rope, const mla_cache *cache, void *workspace, size_t ws_bytes,
+                             void *stream);
 
 /* Bytes of workspace mla_naive_decode needs: the materialised per-head K and V
  * of every visible cached token (B*H*capacity*(d_nope+d_v) bf16) plus the

@@ -177,6 +177,38 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+MLA_API size_t mla_cache_append_workspace_size(const mla_dims *dims, int d_model) {
+    if (check_dims(dims) || d_model < 1) return 0;
+    const int M = dims->B * dims->s_q;
+    const mla::AppendPlan plan = mla::append_plan(M, dims->d_c, d_model);
+    return kStatusBytes + (size_t)plan.splits * M * dims->d_c * sizeof(float);
+}
+
+MLA_API int mla_cache_append(const mla_dims *dims, int d_model, const void *x, const void *w_dkv, const void *k_rope,
+                             const mla_cache *cache, void *workspace, size_t ws_bytes, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    if (d_model < 1) return MLA_ERR_SHAPE;
+    if (d_model % 8) return MLA_ERR_ALIGN;  // rows of x must be whole 16-byte units
+    s = check_cache(dims, cache);
+    if (s) return s;
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    if (ws_bytes < mla_cache_append_workspace_size(dims, d_model)) return MLA_ERR_WORKSPACE;
+    if (dims->B > 0) {
+        if (!x || !w_dkv || (dims->d_rope && !k_rope)) return MLA_ERR_NULL;
+        if (!aligned16(x) || !aligned16(w_dkv) || (k_rope && !aligned16(k_rope))) return MLA_ERR_ALIGN;
+    }
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dims->B == 0) return MLA_OK;
+    mla::AttnParams p = make_params(dims, cache);
+    p.status = (int *)workspace;
+    float *part = (float *)((char *)workspace + kStatusBytes);
+    cudaError_t e = mla::launch_cache_append_tc(p, d_model, x, w_dkv, k_rope, part, st);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_uv, void *out, void *stream) {
     int s = check_dims(dims);
     if (s) return s;

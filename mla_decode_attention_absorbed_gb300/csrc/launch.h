@@ -10,6 +10,21 @@ namespace mla {
 cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void *q_rope, const void *w_uk,
                                void *q_cat, cudaStream_t st);
 cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void *w_uv, void *out, cudaStream_t st);
+// Split-K plan of the cache append's down-projection: 64-column N tiles, and
+// K (d_model, in 64-wide chunks) cut so that all tiles together make about one
+// CTA per SM.  Partials: splits * M * d_c fp32.
+struct AppendPlan {
+    int kc_per_cta, splits;
+};
+inline AppendPlan append_plan(int M, int d_c, int d_model) {
+    const int nk = (d_model + 63) / 64;
+    const int tiles = ((d_c + 63) / 64) * ((M + 127) / 128);
+    int per = (nk * tiles + 147) / 148;
+    if (per < 1) per = 1;
+    return AppendPlan{per, (nk + per - 1) / per};
+}
+cudaError_t launch_cache_append_tc(const AttnParams &p, int d_model, const void *x, const void *w_dkv,
+                                   const void *k_rope, float *part, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams &p, cudaStream_t st);
 cudaError_t launch_naive(const AttnParams &p, int d_nope, int d_v, const void *q_nope, const void *q_rope,

@@ -1,9 +1,13 @@
 // Per-head projection GEMMs on the 5th-generation tensor cores (tcgen05):
 //   absorb:  q_cat[m,h,0:d_c] = q_nope[m,h,:] . W_UK[h]^T          (B operand K-major)
 //   out:     out[m,h,:]       = o_lat[m,h,:]  . W_UV[h]            (B operand MN-major)
-// ("MLA, dim by dim", "MLA Decode": absorb W_UK^T into the current query, and
-// apply W_UV once to the latent-space output.)  m = b*s_q + i runs over the
-// batch's query tokens; one CTA computes a 128-row x BN-column tile of one head.
+//   append:  c[m,:]           = x[m,:] . W_DKV                     (B operand MN-major, split K)
+// ("MLA, dim by dim", "MLA Decode": absorb W_UK^T into the current query, apply
+// W_UV once to the latent-space output, and compress the new token's hidden
+// state into its latent, which is appended to the cache.)  m = b*s_q + i runs
+// over the batch's query tokens; one CTA computes a 128-row x BN-column tile of
+// one head, over all of K or, split K, over a run of K chunks whose fp32 tile
+// it stores as that split's partial.
 //
 // Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns tensor memory
 // and issues the MMAs, warps 2-5 drain the fp32 accumulator from TMEM, round to
@@ -32,6 +36,9 @@ struct ProjArgs {
     int out_row;           // elements per (m, h) output row
     const __nv_bfloat16 *rope_src;  // absorb only: q_rope [M][H][d_rope], copied after column d_c
     int d_rope;
+    float *acc;            // split K: fp32 partials [splits][M][N] instead of `out`
+    int kc_per_cta;        // split K: 64-wide K chunks per CTA
+    int splits;            // split K: CTAs along K (grid z)
 };
 
 template <int BN>
@@ -57,8 +64,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM, h = blockIdx.z;
-    const int nk = (g.K + kBK - 1) / kBK;  // the last chunk's columns past K read as zero
+    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kBM;
+    const int nk_all = (g.K + kBK - 1) / kBK;  // the last chunk's columns past K read as zero
+    const int h = g.acc ? 0 : blockIdx.z;
+    const int kc0 = g.acc ? blockIdx.z * g.kc_per_cta : 0;
+    const int nk = g.acc ? min(g.kc_per_cta, nk_all - kc0) : nk_all;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -88,12 +98,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (*abort_flag) break;
             uint8_t *sa = smem + s * L::kStageBytes;
             uint8_t *sb = sa + L::kABytes;
+            const int kx = (kc0 + kc) * kBK;
             mbar_arrive_expect_tx(&full[s], L::kStageBytes);
-            tma_load_3d(sa, &tmA, &full[s], kc * kBK, h, m0);
+            tma_load_3d(sa, &tmA, &full[s], kx, h, m0);
             if (kBMN) {
-                for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tmB, &full[s], n0 + 64 * j, kc * kBK, h);
+                for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tmB, &full[s], n0 + 64 * j, kx, h);
             } else {
-                tma_load_3d(sb, &tmB, &full[s], kc * kBK, n0, h);
+                tma_load_3d(sb, &tmB, &full[s], kx, n0, h);
             }
         }
     } else if (warp == 1 && lane == 0) {
@@ -125,11 +136,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = q * 32 + lane;
         const int m = m0 + row;
-        const bool ok = mbar_wait(acc_full, 0) && !*abort_flag;
+        const bool ok = (nk <= 0 || mbar_wait(acc_full, 0)) && !*abort_flag;
         tc_fence_after();
-        __nv_bfloat16 *dst = g.out + ((long long)m * g.H + h) * g.out_row + n0;
         const int n_valid = g.N - n0;  // a multiple of 16
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        if (g.acc) {
+            // split K: this CTA's fp32 tile is split blockIdx.z's partial (zeros if it has no K)
+            float *prow = g.acc + ((long long)blockIdx.z * g.M + m) * g.N + n0;
+            for (int c0 = 0; c0 < BN; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(tmem + tmem_lane_base(q) + c0, r);
+                tmem_ld_wait();
+                if (m < g.M && c0 < n_valid) {
+                    float4 *a4 = reinterpret_cast<float4 *>(prow + c0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        a4[e] = nk <= 0 ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                        : make_float4(ok ? __uint_as_float(r[4 * e]) : __int_as_float(0x7fc00000),
+                                                      __uint_as_float(r[4 * e + 1]), __uint_as_float(r[4 * e + 2]),
+                                                      __uint_as_float(r[4 * e + 3]));
+                }
+            }
+        }
+        __nv_bfloat16 *dst = g.acc ? nullptr : g.out + ((long long)m * g.H + h) * g.out_row + n0;
+        for (int c0 = 0; !g.acc && c0 < BN; c0 += 16) {
             uint32_t r[16];
             tmem_ld16(tmem + tmem_lane_base(q) + c0, r);
             tmem_ld_wait();
@@ -146,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
         }
-        if (g.rope_src != nullptr && blockIdx.x == 0 && m < g.M) {
+        if (!g.acc && g.rope_src != nullptr && blockIdx.x == 0 && m < g.M) {
             const uint4 *src = reinterpret_cast<const uint4 *>(g.rope_src + ((long long)m * g.H + h) * g.d_rope);
             uint4 *d = reinterpret_cast<uint4 *>(g.out + ((long long)m * g.H + h) * g.out_row + g.N);
             for (int e = 0; e < g.d_rope / 8; ++e) d[e] = src[e];
@@ -165,7 +194,7 @@ cudaError_t launch_proj(const CUtensorMap &tA, const CUtensorMap &tB, const Proj
     const int smem = ProjSmem<BN>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<BN, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((g.N + BN - 1) / BN, (g.M + kBM - 1) / kBM, g.H);
+    dim3 grid((g.N + BN - 1) / BN, (g.M + kBM - 1) / kBM, g.acc ? g.splits : g.H);
     proj_gemm_tc<BN, kBMN><<<grid, kThreads, smem, st>>>(tA, tB, g);
     return cudaGetLastError();
 }
@@ -193,7 +222,7 @@ cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void
     uint32_t box[3] = {64, (uint32_t)BN, 1};
     if (!encode_bf16_sw128(&tB, w_uk, 3, dims, strides, box)) return cudaErrorInvalidValue;
     ProjArgs g{M, d.H, d.d_c, d.d_nope, (__nv_bfloat16 *)q_cat, d.d_c + d.d_rope,
-               d.d_rope ? (const __nv_bfloat16 *)q_rope : nullptr, d.d_rope};
+               d.d_rope ? (const __nv_bfloat16 *)q_rope : nullptr, d.d_rope, nullptr, 0, 1};
     switch (BN) {
         case 256: return launch_proj<256, false>(tA, tB, g, st);
         case 192: return launch_proj<192, false>(tA, tB, g, st);
@@ -213,7 +242,7 @@ cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void 
     uint64_t strides[2] = {(uint64_t)d.d_v * 2, (uint64_t)d.d_c * d.d_v * 2};
     uint32_t box[3] = {64, 64, 1};
     if (!encode_bf16_sw128(&tB, w_uv, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    ProjArgs g{M, d.H, d.d_v, d.d_c, (__nv_bfloat16 *)out, d.d_v, nullptr, 0};
+    ProjArgs g{M, d.H, d.d_v, d.d_c, (__nv_bfloat16 *)out, d.d_v, nullptr, 0, nullptr, 0, 1};
     switch ((d.d_v + 63) / 64 * 64) {  // MMA width: d_v rounded up to whole 64-column boxes
         case 256: return launch_proj<256, true>(tA, tB, g, st);
         case 192: return launch_proj<192, true>(tA, tB, g, st);
@@ -221,6 +250,76 @@ cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void 
         case 64: return launch_proj<64, true>(tA, tB, g, st);
         default: return cudaErrorNotSupported;
     }
+}
+
+// Writes row m = b*s_q + i of the new latents (the sum of the splits' fp32
+// partials, rounded to bf16) and its RoPE key into the cache at position
+// L_b - s_q + i, contiguous or paged.  One CTA per row: 64 threads per group of
+// 8-column chunks, four groups each summing every fourth split, summed through
+// shared memory (the partials' loads are independent, not one chain).
+constexpr int kScatterThreads = 256;
+__global__ void __launch_bounds__(kScatterThreads) append_scatter(AttnParams p, const float *part, int splits,
+                                                                  const __nv_bfloat16 *k_rope) {
+    __shared__ float red[3][512];
+    const int m = blockIdx.x;
+    const int M = p.B * p.s_q;
+    const int b = m / p.s_q, i = m % p.s_q;
+    const int L = __ldg(p.seq_lens + b);
+    if (!seq_len_ok(p, L)) {
+        if (threadIdx.x == 0) set_status(p.status, MLA_ERR_SEQLEN);
+        return;
+    }
+    const __nv_bfloat16 *row = kv_row(p, b, L - p.s_q + i);
+    if (row == nullptr) {
+        if (threadIdx.x == 0) set_status(p.status, MLA_ERR_PAGE);
+        return;
+    }
+    __nv_bfloat16 *dst = const_cast<__nv_bfloat16 *>(row);
+    const int grp = threadIdx.x / 64, c = 8 * (threadIdx.x % 64);  // d_c <= 512: one chunk per thread
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (c < p.d_c) {
+        for (int s = grp; s < splits; s += 4) {
+            const float *src = part + ((long long)s * M + m) * p.d_c + c;
+            const float4 u = *reinterpret_cast<const float4 *>(src);
+            const float4 w = *reinterpret_cast<const float4 *>(src + 4);
+            a[0] += u.x; a[1] += u.y; a[2] += u.z; a[3] += u.w;
+            a[4] += w.x; a[5] += w.y; a[6] += w.z; a[7] += w.w;
+        }
+        if (grp > 0)
+            for (int e = 0; e < 8; ++e) red[grp - 1][c + e] = a[e];
+    }
+    __syncthreads();
+    if (grp == 0 && c < p.d_c) {
+        for (int e = 0; e < 8; ++e) a[e] += red[0][c + e] + red[1][c + e] + red[2][c + e];
+        *reinterpret_cast<uint4 *>(dst + c) = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                                          pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+    }
+    if (grp == 1 && c < p.d_rope)
+        *reinterpret_cast<uint4 *>(dst + p.d_c + c) =
+            *reinterpret_cast<const uint4 *>(k_rope + (long long)m * p.d_rope + c);
+}
+
+// c = x . W_DKV for the batch's new tokens, appended with their RoPE keys.  The
+// GEMM is weight-bound (every W_DKV byte read once), so K is split over enough
+// CTAs to stream the weight at full bandwidth (append_splits); each split stores
+// its fp32 partial tile in `part`, and the scatter sums them into the cache rows.
+cudaError_t launch_cache_append_tc(const AttnParams &p, int d_model, const void *x, const void *w_dkv,
+                                   const void *k_rope, float *part, cudaStream_t st) {
+    const int M = p.B * p.s_q;
+    if (M == 0) return cudaSuccess;
+    CUtensorMap tA, tB;
+    if (!map_rows(&tA, x, M, 1, d_model)) return cudaErrorInvalidValue;
+    // W_DKV [d_model][d_c]: MN-major B, box 64 (n) x 64 (k) x 1
+    uint64_t dims[3] = {(uint64_t)p.d_c, (uint64_t)d_model, 1};
+    uint64_t strides[2] = {(uint64_t)p.d_c * 2, (uint64_t)d_model * p.d_c * 2};
+    uint32_t box[3] = {64, 64, 1};
+    if (!encode_bf16_sw128(&tB, w_dkv, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    const AppendPlan plan = append_plan(M, p.d_c, d_model);
+    ProjArgs g{M, 1, p.d_c, d_model, nullptr, 0, nullptr, 0, part, plan.kc_per_cta, plan.splits};
+    cudaError_t e = launch_proj<64, true>(tA, tB, g, st);
+    if (e != cudaSuccess) return e;
+    append_scatter<<<M, kScatterThreads, 0, st>>>(p, part, plan.splits, (const __nv_bfloat16 *)k_rope);
+    return cudaGetLastError();
 }
 
 }  // namespace mla

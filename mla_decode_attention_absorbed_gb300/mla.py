@@ -37,7 +37,8 @@ class Cache(ctypes.Structure):
 
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_workspace_size",
            "mla_decode_num_splits", "mla_decode_attn", "mla_out_proj", "mla_naive_workspace_size",
-           "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc")
+           "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc", "mla_cache_append_workspace_size",
+           "mla_cache_append")
 
 
 def lib_path() -> str:
@@ -72,6 +73,10 @@ def load(path: str | None = None):
     lib.mla_naive_workspace_size.restype = SZ
     lib.mla_naive_decode.argtypes = [pd, P, P, pc, P, P, P, P, P, SZ, P]
     lib.mla_naive_decode.restype = I
+    lib.mla_cache_append_workspace_size.argtypes = [pd, I]
+    lib.mla_cache_append_workspace_size.restype = SZ
+    lib.mla_cache_append.argtypes = [pd, I, P, P, P, pc, P, SZ, P]
+    lib.mla_cache_append.restype = I
     lib.mla_read_status.argtypes = [P, ctypes.POINTER(I), P]
     lib.mla_read_status.restype = I
     lib.mla_decode_attn_noalloc.argtypes = [pd, P, pc, P, P, I, P, P]
@@ -193,6 +198,27 @@ def out_proj(prob: Problem, o_lat, w_uv, out=None, stream=None):
     _check(lib.mla_out_proj(ctypes.byref(d), _ptr(o_lat), _ptr(w_uv), _ptr(out), _stream(stream)),
            "mla_out_proj")
     return out
+
+
+def cache_append_workspace_size(prob: Problem, d_model: int) -> int:
+    d = prob.dims()
+    n = load().mla_cache_append_workspace_size(ctypes.byref(d), int(d_model))
+    if n == 0:
+        raise ValueError("mla_cache_append_workspace_size rejected the arguments")
+    return int(n)
+
+
+def cache_append(prob: Problem, x, w_dkv, k_rope, cache: Cache, workspace=None, stream=None):
+    """mla_cache_append: c = x . W_DKV of the new tokens, written with k_rope into
+    rows seq_lens[b] - s_q + i of the cache (whose kv buffer is modified)."""
+    lib = load()
+    if workspace is None:
+        workspace = alloc_workspace(cache_append_workspace_size(prob, int(x.shape[-1])), x.device)
+    d = prob.dims()
+    _check(lib.mla_cache_append(ctypes.byref(d), int(x.shape[-1]), _ptr(x), _ptr(w_dkv), _ptr(k_rope),
+                                ctypes.byref(cache), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mla_cache_append")
+    return workspace
 
 
 def naive_workspace_size(prob: Problem, cache: Cache) -> int:

@@ -134,3 +134,19 @@ def make_inputs(cfg: MLAConfig, seq_lens=None) -> dict:
     return dict(q_nope=q_nope, q_rope=q_rope, kv=kv, w_uk=w_uk, w_uv=w_uv, seq_lens=lens,
                 block_table=block_table, page_size=cfg.page_size,
                 T_max=(kv.shape[1] if not cfg.paged else block_table.shape[1] * cfg.page_size))
+
+
+def make_append_inputs(cfg: MLAConfig, d_model: int, seed: int = 7) -> dict:
+    """Inputs of the cache-append step (latent down-projection of the new tokens).
+
+    One CPU generator seeded with ``seed``; draws in this order, each fp32
+    ``randn`` rounded to bf16:
+      1. x [B, s_q, d_model]      ~ N(0, 1)        (the new tokens' hidden states)
+      2. W_DKV [d_model, d_c]     ~ N(0, 1 / d_model)
+      3. k_rope [B, s_q, d_rope]  ~ N(0, 1)        (their RoPE keys, already rotated)"""
+    g = torch.Generator().manual_seed(seed)
+    x = _randn_bf16(g, (cfg.B, cfg.s_q, d_model))
+    w_dkv = _randn_bf16(g, (d_model, cfg.d_c), std=1.0 / math.sqrt(d_model))
+    k_rope = _randn_bf16(g, (cfg.B, cfg.s_q, cfg.d_rope))
+    return dict(x=x, w_dkv=w_dkv, k_rope=k_rope, d_model=d_model)
+

@@ -76,6 +76,7 @@ def _load():
             lib.orc_out_proj.argtypes = [ctypes.POINTER(_Dims), P, P, P]
             lib.orc_naive.argtypes = [ctypes.POINTER(_Dims), P, P, ctypes.POINTER(_Cache), P, P,
                                       P, LL, P, P]
+            lib.orc_down_proj.argtypes = [LL, ctypes.c_int, ctypes.c_int, P, P, P]
             _lib = lib
     return _lib
 
@@ -200,6 +201,52 @@ def out_proj(d, o_lat, w_uv) -> torch.Tensor:
     out = torch.empty(d.B, d.s_q, d.H, d.d_v, dtype=torch.float64)
     lib.orc_out_proj(ctypes.byref(_dims(d)), _ptr(o), _ptr(wv), _ptr(out))
     return out
+
+
+def down_proj(x, w_dkv) -> torch.Tensor:
+    """c = x . W_DKV in fp64: x [..., d_model] bf16, w_dkv [d_model, d_c] bf16 -> [..., d_c]."""
+    lib = _load()
+    xb, wb = _bits(x), _bits(w_dkv)
+    d_model, d_c = int(w_dkv.shape[0]), int(w_dkv.shape[1])
+    M = xb.numel() // d_model
+    c = torch.empty(M, d_c, dtype=torch.float64)
+    lib.orc_down_proj(M, d_model, d_c, _ptr(xb), _ptr(wb), _ptr(c))
+    return c.view(*x.shape[:-1], d_c)
+
+
+def cache_append(d, x, w_dkv, k_rope, kv, seq_lens, block_table=None, page_size=64):
+    """The cache after appending the new tokens, in fp64, and a bool mask of the
+    rows written ("MLA, dim by dim", "MLA Decode": c = x . W_DKV is appended).
+
+    Token i of sequence b (x [B, s_q, d_model], k_rope [B, s_q, d_rope]) lands at
+    position L_b - s_q + i (seq_lens already count the new tokens): row
+    [c | k_rope] of the contiguous cache [B, T_max, W], or of page
+    block_table[b][pos // page_size] of the pool [P, page_size, W].  Invalid
+    lengths or page ids write nothing."""
+    c = down_proj(x, w_dkv)
+    out = kv.detach().to("cpu", torch.float64).clone()
+    written = torch.zeros(out.shape[:-1], dtype=torch.bool)
+    kr = k_rope.detach().to("cpu", torch.float64)
+    lens = [int(v) for v in seq_lens.detach().to("cpu")]
+    bt = block_table.detach().to("cpu") if block_table is not None else None
+    cap = int(bt.shape[1]) * page_size if bt is not None else int(kv.shape[1])
+    for b in range(d.B):
+        L = lens[b]
+        if L < d.s_q or L > cap:
+            continue
+        for i in range(d.s_q):
+            pos = L - d.s_q + i
+            if bt is None:
+                idx = (b, pos)
+            else:
+                page = int(bt[b, pos // page_size])
+                if page < 0 or page >= int(kv.shape[0]):
+                    continue
+                idx = (page, pos % page_size)
+            out[idx][: d.d_c] = c[b, i]
+            out[idx][d.d_c:] = kr[b, i]
+            written[idx] = True
+    return out, written
 
 
 def naive(d, q_nope, q_rope, kv, seq_lens, w_uk, w_uv, block_table=None, page_size=64, rows=None):

@@ -290,6 +290,25 @@ void orc_out_proj(const orc_dims *d, const double *o_lat, const uint16_t *w_uv, 
     }
 }
 
+/* Latent down-projection of the new tokens ([MLA-dim] "MLA Decode": the
+ * current token's hidden state is compressed, x . W_DKV -> c^KV of width d_c, and
+ * appended to the cache; [AI] 4.1, the 2 d_model d_c FLOPs of F_fixed):
+ *     c[m,k] = sum_i x[m,i] * W_DKV[i,k]
+ * Layouts: x [M][d_model], W_DKV [d_model][d_c], c [M][d_c]. */
+void orc_down_proj(long long M, int d_model, int d_c, const uint16_t *x, const uint16_t *w_dkv, double *c)
+{
+#pragma omp parallel for schedule(static)
+    for (long long m = 0; m < M; ++m) {
+        double *out = c + m * d_c;
+        for (int k = 0; k < d_c; ++k) out[k] = 0.0;
+        for (int i = 0; i < d_model; ++i) {
+            double a = bf16_to_f64(x[m * d_model + i]);
+            const uint16_t *wrow = w_dkv + (long long)i * d_c;
+            for (int k = 0; k < d_c; ++k) out[k] += a * bf16_to_f64(wrow[k]);
+        }
+    }
+}
+
 /* Naive decompress-then-attend ([speedup] "The naive form, written out";
  * [AI] 3.3; [intens] decompression cost): every visible cached latent of the
  * sequence is up-projected per head,

@@ -23,7 +23,7 @@ import torch.nn.functional as F
 
 import oracle
 from oracle import counts
-from mla_decode_attention_absorbed_gb300.workloads import MLAConfig, make_inputs
+from mla_decode_attention_absorbed_gb300.workloads import MLAConfig, make_append_inputs, make_inputs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.json")
 
@@ -352,3 +352,96 @@ def test_split_and_merge_equals_whole():
 def test_merge_of_nothing():
     o, lse = oracle.combine([float("-inf")] * 2, [0.0, 0.0], torch.zeros(2, 4, dtype=torch.float64))
     assert lse == float("-inf") and torch.equal(o, torch.zeros(4, dtype=torch.float64))
+
+
+# ----------------------------------------------------------------------------- cache append
+# "MLA, dim by dim", "MLA Decode": the new token's hidden state is compressed,
+# x . W_DKV -> c^KV (2 d d_c FLOPs), and appended to the latent cache.
+
+def test_down_proj_selection_matrix():
+    """A one-hot W_DKV picks columns of x: c[m, k] = x[m, perm[k]] exactly."""
+    g = torch.Generator().manual_seed(3)
+    d_model, d_c = 40, 16
+    x = torch.randn(3, 2, d_model, generator=g).bfloat16()
+    perm = torch.randperm(d_model, generator=g)[:d_c]
+    w = torch.zeros(d_model, d_c)
+    w[perm, torch.arange(d_c)] = 1.0
+    c = oracle.down_proj(x, w.bfloat16())
+    assert torch.equal(c, x.double()[..., perm])
+
+
+def test_down_proj_linearity():
+    """c is linear in x: c(2 x1 - x2) = 2 c(x1) - c(x2) to rounding of the fp64 sums."""
+    g = torch.Generator().manual_seed(4)
+    x1 = torch.randint(-8, 8, (4, 24), generator=g).float().bfloat16()
+    x2 = torch.randint(-8, 8, (4, 24), generator=g).float().bfloat16()
+    w = (torch.randint(-8, 8, (24, 8), generator=g).float() / 8).bfloat16()
+    lhs = oracle.down_proj((2 * x1.float() - x2.float()).bfloat16(), w)
+    rhs = 2 * oracle.down_proj(x1, w) - oracle.down_proj(x2, w)
+    assert torch.equal(lhs, rhs)  # small integers and eighths: every sum is exact
+
+
+def _append_case(paged: bool, s_q: int = 2):
+    cfg = MLAConfig("append_pin", B=3, H=4, d_c=64, d_rope=16, d_nope=32, d_v=32, s_q=s_q,
+                    len_lo=5, len_hi=150, paged=paged, page_size=64, seed=11, canary=False)
+    inp = make_inputs(cfg)
+    app = make_append_inputs(cfg, d_model=48)
+    new, written = oracle.cache_append(cfg, app["x"], app["w_dkv"], app["k_rope"], inp["kv"], inp["seq_lens"],
+                                       inp["block_table"], cfg.page_size)
+    return cfg, inp, app, new, written
+
+
+def _logical_rows(cfg, inp, cache64):
+    """[b][j] -> fp64 row of token j of sequence b (contiguous or through the block table)."""
+    out = {}
+    for b in range(cfg.B):
+        L = int(inp["seq_lens"][b])
+        for j in range(L):
+            if inp["block_table"] is None:
+                out[(b, j)] = cache64[b, j]
+            else:
+                page = int(inp["block_table"][b, j // cfg.page_size])
+                out[(b, j)] = cache64[page, j % cfg.page_size]
+    return out
+
+
+def test_append_writes_the_new_positions_only():
+    for paged in (False, True):
+        cfg, inp, app, new, written = _append_case(paged)
+        old = inp["kv"].double()
+        c = oracle.down_proj(app["x"], app["w_dkv"])
+        rows = _logical_rows(cfg, inp, new)
+        n_new = 0
+        for b in range(cfg.B):
+            L = int(inp["seq_lens"][b])
+            for i in range(cfg.s_q):
+                r = rows[(b, L - cfg.s_q + i)]
+                assert torch.equal(r[:cfg.d_c], c[b, i])
+                assert torch.equal(r[cfg.d_c:], app["k_rope"][b, i].double())
+                n_new += 1
+        assert int(written.sum()) == n_new
+        assert torch.equal(new[~written], old[~written])
+
+
+def test_append_paged_equals_contiguous():
+    cfg_c, inp_c, _, new_c, _ = _append_case(False)
+    cfg_p, inp_p, _, new_p, _ = _append_case(True)
+    # same lengths (same seed, same draw order for the lengths)
+    assert torch.equal(inp_c["seq_lens"], inp_p["seq_lens"])
+    rc, rp = _logical_rows(cfg_c, inp_c, new_c), _logical_rows(cfg_p, inp_p, new_p)
+    for b in range(cfg_c.B):
+        L = int(inp_c["seq_lens"][b])
+        for i in range(cfg_c.s_q):
+            assert torch.equal(rc[(b, L - cfg_c.s_q + i)], rp[(b, L - cfg_c.s_q + i)])
+
+
+def test_append_skips_invalid_lengths_and_pages():
+    cfg, inp, app, _, _ = _append_case(True, s_q=1)
+    lens = inp["seq_lens"].clone()
+    lens[0] = 0                      # shorter than s_q
+    bt = inp["block_table"].clone()
+    L1 = int(lens[1])
+    bt[1, (L1 - 1) // cfg.page_size] = 10 ** 6  # page outside the pool
+    new, written = oracle.cache_append(cfg, app["x"], app["w_dkv"], app["k_rope"], inp["kv"], lens, bt,
+                                       cfg.page_size)
+    assert int(written.sum()) == cfg.B - 2
