@@ -150,3 +150,25 @@ def make_append_inputs(cfg: MLAConfig, d_model: int, seed: int = 7) -> dict:
     k_rope = _randn_bf16(g, (cfg.B, cfg.s_q, cfg.d_rope))
     return dict(x=x, w_dkv=w_dkv, k_rope=k_rope, d_model=d_model)
 
+
+def make_sparse_indices(cfg: MLAConfig, seq_lens: torch.Tensor, topk: int, seed: int = 13) -> torch.Tensor:
+    """Top-k token lists of the sparse decode, int32 [B, s_q, topk].
+
+    Stands in for a learned selector (which needs trained weights): for every
+    sequence b and query token i, ``topk`` distinct positions drawn uniformly
+    from the tokens it may see (0 .. L_b - s_q + i), listed in increasing order;
+    when fewer are visible, all of them, padded with -1.  One CPU generator
+    seeded with ``seed``; one ``randperm`` per (b, i) in that order."""
+    g = torch.Generator().manual_seed(seed)
+    out = torch.full((cfg.B, cfg.s_q, topk), -1, dtype=torch.int32)
+    for b in range(cfg.B):
+        L = int(seq_lens[b])
+        for i in range(cfg.s_q):
+            n_vis = max(0, L - cfg.s_q + i + 1)
+            if n_vis == 0:
+                continue
+            pick = torch.randperm(n_vis, generator=g)[:topk]
+            pick, _ = torch.sort(pick)
+            out[b, i, : pick.numel()] = pick.to(torch.int32)
+    return out
+

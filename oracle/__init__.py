@@ -77,6 +77,8 @@ def _load():
             lib.orc_naive.argtypes = [ctypes.POINTER(_Dims), P, P, ctypes.POINTER(_Cache), P, P,
                                       P, LL, P, P]
             lib.orc_down_proj.argtypes = [LL, ctypes.c_int, ctypes.c_int, P, P, P]
+            lib.orc_attend_sparse.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache), P, ctypes.c_int,
+                                              P, LL, P, P]
             _lib = lib
     return _lib
 
@@ -164,6 +166,24 @@ def attend(d, q_cat, kv, seq_lens, block_table=None, page_size=64, rows=None):
     lse = torch.full((d.B, d.s_q, d.H), float("nan"), dtype=torch.float64)
     r, n = _rows_arg(rows)
     lib.orc_attend(ctypes.byref(_dims(d)), _ptr(q), ctypes.byref(ca.c), _ptr(r), n, _ptr(o), _ptr(lse))
+    return o, lse
+
+
+def attend_sparse(d, q_cat, kv, seq_lens, indices, block_table=None, page_size=64, rows=None):
+    """Sparse top-k attention: (o_lat, lse) float64 over the listed tokens only.
+
+    ``indices`` [B, s_q, topk] int32: token positions per query token, shared by
+    the heads; entries that do not name a visible token (e.g. -1) take no part."""
+    lib = _load()
+    q = _f64(q_cat)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    idx = _i32(indices)
+    topk = int(idx.shape[-1])
+    o = torch.full((d.B, d.s_q, d.H, d.d_c), float("nan"), dtype=torch.float64)
+    lse = torch.full((d.B, d.s_q, d.H), float("nan"), dtype=torch.float64)
+    r, n = _rows_arg(rows)
+    lib.orc_attend_sparse(ctypes.byref(_dims(d)), _ptr(q), ctypes.byref(ca.c), _ptr(idx), topk, _ptr(r), n,
+                          _ptr(o), _ptr(lse))
     return o, lse
 
 

@@ -203,6 +203,76 @@ void orc_attend(const orc_dims *d, const double *q_cat, const orc_cache *c,
     }
 }
 
+/* Sparse top-k attention ([AI] 6: a selector keeps k cached tokens per query
+ * token, they are gathered by index and the scoring and the weighted sum run
+ * over them only): row r = (b*s_q + i)*H + h attends over the entries
+ * idx[b][i][0 .. topk) that name a visible token (0 <= j <= L - s_q + i;
+ * other entries, such as -1 padding, take no part), each entry as listed,
+ * with the same score and latent-space sum as orc_attend.  A row with no
+ * visible entry gets o_lat = 0 and lse = -inf. */
+static void attend_row_sparse(const orc_dims *d, const double *q_cat, const orc_cache *c,
+                              const int32_t *idx, int topk, long long r, double *scores,
+                              double *o_lat, double *lse)
+{
+    long long bi = r / d->H;
+    int i = (int)(bi % d->s_q);
+    int b = (int)(bi / d->s_q);
+    long long wq = (long long)d->d_c + d->d_rope;
+    const double *q = q_cat + r * wq;
+    double *o = o_lat + r * d->d_c;
+    if (!row_is_valid(d, c, b)) {
+        for (int k = 0; k < d->d_c; ++k) o[k] = NAN;
+        lse[r] = NAN;
+        return;
+    }
+    long long lim = c->seq_lens[b] - d->s_q + i;
+    const int32_t *list = idx + bi * topk;
+    double m = -INFINITY;
+    for (int e = 0; e < topk; ++e) {
+        long long j = list[e];
+        scores[e] = -INFINITY;
+        if (j < 0 || j > lim) continue;
+        const uint16_t *t = token_row(d, c, b, j);
+        double dot = 0.0;
+        for (long long k = 0; k < wq; ++k)
+            dot += q[k] * bf16_to_f64(t[k]);
+        scores[e] = d->scale * dot;
+        if (scores[e] > m) m = scores[e];
+    }
+    for (int k = 0; k < d->d_c; ++k) o[k] = 0.0;
+    if (m == -INFINITY) {
+        lse[r] = -INFINITY;
+        return;
+    }
+    double sum = 0.0;
+    for (int e = 0; e < topk; ++e)
+        if (scores[e] != -INFINITY) sum += exp(scores[e] - m);
+    double l = m + log(sum);
+    for (int e = 0; e < topk; ++e) {
+        if (scores[e] == -INFINITY) continue;
+        double p = exp(scores[e] - l);
+        const uint16_t *t = token_row(d, c, b, list[e]);
+        for (int k = 0; k < d->d_c; ++k)
+            o[k] += p * bf16_to_f64(t[k]);
+    }
+    lse[r] = l;
+}
+
+void orc_attend_sparse(const orc_dims *d, const double *q_cat, const orc_cache *c,
+                       const int32_t *idx, int topk, const long long *rows, long long n_rows,
+                       double *o_lat, double *lse)
+{
+    long long total = rows ? n_rows : (long long)d->B * d->s_q * d->H;
+#pragma omp parallel
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(topk > 0 ? topk : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (long long t = 0; t < total; ++t)
+            attend_row_sparse(d, q_cat, c, idx, topk, rows ? rows[t] : t, scores, o_lat, lse);
+        free(scores);
+    }
+}
+
 /* Unnormalised partial over the visible tokens of row r that fall in [j0, j1):
  * m = max s_j (-inf if none), l = sum exp(s_j - m), acc[c] = sum exp(s_j - m) c_kv[j,c].
  * Used to pin the cross-split merge below. */

@@ -23,7 +23,7 @@ import torch.nn.functional as F
 
 import oracle
 from oracle import counts
-from mla_decode_attention_absorbed_gb300.workloads import MLAConfig, make_append_inputs, make_inputs
+from mla_decode_attention_absorbed_gb300.workloads import MLAConfig, make_append_inputs, make_inputs, make_sparse_indices
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "page_figures.json")
 
@@ -445,3 +445,73 @@ def test_append_skips_invalid_lengths_and_pages():
     new, written = oracle.cache_append(cfg, app["x"], app["w_dkv"], app["k_rope"], inp["kv"], lens, bt,
                                        cfg.page_size)
     assert int(written.sum()) == cfg.B - 2
+
+
+# ----------------------------------------------------------------------------- sparse top-k decode
+# "Why MLA and MTP Fight Each Other", 6: the selected tokens are gathered by
+# index and the scoring and the weighted sum run over those only.
+
+def _sparse_case(s_q=2, paged=False):
+    cfg = MLAConfig("sparse_pin", B=3, H=4, d_c=64, d_rope=16, d_nope=32, d_v=32, s_q=s_q,
+                    len_lo=40, len_hi=130, paged=paged, seed=21, canary=True)
+    inp = make_inputs(cfg)
+    q_cat = oracle.absorb_q(cfg, inp["q_nope"], inp["q_rope"], inp["w_uk"]).to(torch.bfloat16)
+    return cfg, inp, q_cat
+
+
+def _full_lists(cfg, lens, extra=0):
+    """Every visible token of every (b, i), in order, padded with -1 (plus `extra` pads)."""
+    topk = int(lens.max()) + extra
+    idx = torch.full((cfg.B, cfg.s_q, topk), -1, dtype=torch.int32)
+    for b in range(cfg.B):
+        for i in range(cfg.s_q):
+            n = int(lens[b]) - cfg.s_q + i + 1
+            idx[b, i, :n] = torch.arange(n, dtype=torch.int32)
+    return idx
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_sparse_with_every_token_is_dense(paged):
+    cfg, inp, q = _sparse_case(paged=paged)
+    idx = _full_lists(cfg, inp["seq_lens"], extra=5)
+    o_s, l_s = oracle.attend_sparse(cfg, q, inp["kv"], inp["seq_lens"], idx, inp["block_table"], cfg.page_size)
+    o_d, l_d = oracle.attend(cfg, q, inp["kv"], inp["seq_lens"], inp["block_table"], cfg.page_size)
+    assert torch.allclose(o_s, o_d, rtol=0, atol=1e-12) and torch.allclose(l_s, l_d, rtol=0, atol=1e-12)
+
+
+def test_sparse_order_padding_and_future_entries_do_not_matter():
+    cfg, inp, q = _sparse_case()
+    lens = inp["seq_lens"]
+    idx = make_sparse_indices(cfg, lens, topk=24)
+    o0, l0 = oracle.attend_sparse(cfg, q, inp["kv"], lens, idx)
+    g = torch.Generator().manual_seed(5)
+    perm = torch.randperm(idx.shape[-1], generator=g)
+    o1, l1 = oracle.attend_sparse(cfg, q, inp["kv"], lens, idx[..., perm])
+    assert torch.allclose(o0, o1, atol=1e-12) and torch.allclose(l0, l1, atol=1e-12)
+    # -1 padding and entries past the causal limit (future tokens, NaN canaries) take no part
+    fut = torch.empty(cfg.B, cfg.s_q, 3, dtype=torch.int32)
+    for b in range(cfg.B):
+        for i in range(cfg.s_q):
+            fut[b, i] = torch.tensor([-1, int(lens[b]) - cfg.s_q + i + 1, int(lens[b]) + 7])
+    o2, l2 = oracle.attend_sparse(cfg, q, inp["kv"], lens, torch.cat([idx, fut], dim=-1))
+    assert torch.allclose(o0, o2, atol=1e-12) and torch.allclose(l0, l2, atol=1e-12)
+
+
+def test_sparse_single_token_is_that_latent():
+    cfg, inp, q = _sparse_case(s_q=1)
+    lens = inp["seq_lens"]
+    idx = torch.full((cfg.B, 1, 4), -1, dtype=torch.int32)
+    idx[:, 0, 2] = 3
+    o, lse = oracle.attend_sparse(cfg, q, inp["kv"], lens, idx)
+    for b in range(cfg.B):
+        row = inp["kv"][b, 3].double()
+        assert torch.equal(o[b, 0], row[:cfg.d_c].expand(cfg.H, -1))
+        s = cfg.scale * (q[b, 0].double() @ row)
+        assert torch.allclose(lse[b, 0], s, atol=1e-12)
+
+
+def test_sparse_no_visible_entry_gives_zero_and_minus_inf():
+    cfg, inp, q = _sparse_case(s_q=1)
+    idx = torch.full((cfg.B, 1, 8), -1, dtype=torch.int32)
+    o, lse = oracle.attend_sparse(cfg, q, inp["kv"], inp["seq_lens"], idx)
+    assert torch.equal(o, torch.zeros_like(o)) and bool(torch.isneginf(lse).all())
