@@ -12,6 +12,8 @@
  *                    over a contiguous or paged latent cache, split along the
  *                    history and merged with a log-sum-exp combine
  *   mla_out_proj     out = o_lat . W_UV                               per head
+ *   mla_decode_attn_sparse  the same attention over k listed cached tokens
+ *                    per query token (sparse top-k decode)
  *   mla_cache_append c_kv = x . W_DKV of the new tokens, written with their
  *                    (already rotated) RoPE keys into the latent cache
  *   mla_naive_decode the decompress-then-attend form, a comparison point only
@@ -149,6 +151,28 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
  * o_lat [B][s_q][H][d_c], w_uv [H][d_c][d_v], out [B][s_q][H][d_v]. */
 MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_uv,
                          void *out, void *stream);
+
+/* Bytes of workspace mla_decode_attn_sparse needs for this problem, list length
+ * and split count (0 = the library's choice).  Returns 0 for invalid arguments. */
+MLA_API size_t mla_decode_sparse_workspace_size(const mla_dims *dims, const mla_cache *cache, int topk,
+                                                int num_splits);
+
+/* Sparse top-k decode ("Why MLA and MTP Fight Each Other", 6: a selector keeps
+ * k cached tokens per query token; the latents are gathered by index and the
+ * scoring and the weighted sum run over those only, so the cost is flat in the
+ * history length).  Same inputs, outputs, workspace and status word as
+ * mla_decode_attn, plus indices int32 [B][s_q][topk] (device): the token
+ * positions each query token attends to, shared by all heads.  An entry takes
+ * part when it names a token the query may see (0 <= j <= L_b - s_q + i) on a
+ * page inside the pool; others (e.g. -1 padding, future tokens) are skipped,
+ * and a query with no such entry gets o_lat = 0 and lse = -inf.  Each entry
+ * counts once per listing.  The learned selector itself is not part of the
+ * library.  Requires s_q == 1 or H a multiple of 128 (every 128-row block of
+ * query rows belongs to one query token), and, for a contiguous cache,
+ * seq_stride a multiple of d_c + d_rope; otherwise MLA_ERR_UNSUPPORTED. */
+MLA_API int mla_decode_attn_sparse(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
+                                   const int *indices, int topk, void *o_lat, float *lse, void *workspace,
+                                   size_t ws_bytes, int num_splits, void *stream);
 
 /* Bytes of workspace mla_cache_append needs: the status word (256 B) and the
  * fp32 partial sums of the split down-projection (a few MB at DeepSeek-V3

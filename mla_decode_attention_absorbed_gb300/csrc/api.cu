@@ -55,9 +55,10 @@ int check_cache(const mla_dims *d, const mla_cache *c) {
     return MLA_OK;
 }
 
-int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
+// maxL: the longest token range one work item streams (sequence length, or the
+// sparse list length)
+int plan_splits_len(const mla_dims *d, long long maxL, int requested) {
     if (requested > 0) return requested;
-    long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
     long long tiles = (maxL + 63) / 64;
     long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
     long long units = (long long)d->B * row_blocks;  // work items before splitting
@@ -73,6 +74,22 @@ int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
     if (want < 1) want = 1;
     if (want > kMaxSplits) want = kMaxSplits;
     return (int)want;
+}
+
+int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
+    return plan_splits_len(d, c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c), requested);
+}
+
+// Sparse decode: the index list must be shared by all rows of a 128-row block
+// (one query token per block, or a single query token), and the contiguous
+// cache must be a stack of whole rows (gathered through a 2-D view).
+int check_sparse(const mla_dims *d, const mla_cache *c, const int *indices, int topk) {
+    if (topk < 1) return MLA_ERR_SHAPE;
+    if (d->s_q > 1 && d->H % 128) return MLA_ERR_UNSUPPORTED;
+    if (!c->block_table && c->seq_stride % (d->d_c + d->d_rope)) return MLA_ERR_UNSUPPORTED;
+    if (d->B > 0 && !indices) return MLA_ERR_NULL;
+    if ((uintptr_t)indices & 3u) return MLA_ERR_ALIGN;
+    return MLA_OK;
 }
 
 size_t attn_workspace_bytes(const mla_dims *d, int splits) {
@@ -206,6 +223,51 @@ MLA_API int mla_cache_append(const mla_dims *dims, int d_model, const void *x, c
     p.status = (int *)workspace;
     float *part = (float *)((char *)workspace + kStatusBytes);
     cudaError_t e = mla::launch_cache_append_tc(p, d_model, x, w_dkv, k_rope, part, st);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API size_t mla_decode_sparse_workspace_size(const mla_dims *dims, const mla_cache *cache, int topk,
+                                                int num_splits) {
+    if (check_dims(dims) || check_cache(dims, cache) || topk < 1) return 0;
+    return attn_workspace_bytes(dims, plan_splits_len(dims, topk, num_splits));
+}
+
+MLA_API int mla_decode_attn_sparse(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
+                                   const int *indices, int topk, void *o_lat, float *lse, void *workspace,
+                                   size_t ws_bytes, int num_splits, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    s = check_cache(dims, cache);
+    if (s) return s;
+    s = check_sparse(dims, cache, indices, topk);
+    if (s) return s;
+    if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    const int splits = plan_splits_len(dims, topk, num_splits);
+    if (ws_bytes < attn_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    if (dims->B > 0) {
+        if (!q_cat || !o_lat || !lse) return MLA_ERR_NULL;
+        if (!aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse)) return MLA_ERR_ALIGN;
+    }
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dims->B == 0) return MLA_OK;
+    mla::AttnParams p = make_params(dims, cache);
+    p.q_cat = (const __nv_bfloat16 *)q_cat;
+    p.o_lat = (__nv_bfloat16 *)o_lat;
+    p.lse = lse;
+    p.num_splits = splits;
+    p.status = (int *)workspace;
+    p.indices = indices;
+    p.topk = topk;
+    if (splits > 1) {
+        size_t rows = (size_t)dims->B * splits * dims->s_q * dims->H;
+        char *base = (char *)workspace + kStatusBytes;
+        p.part_ml = (float *)base;
+        p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
+    }
+    cudaError_t e = mla::launch_attn_tc(p, st);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -78,6 +78,8 @@ struct Smem {
     // tile maxima in the loop, softmax sums in the epilogue
     float pair[2][2][kRows];
     int pair_stop[4][2];  // each quadrant's joint decision to leave the tile loop, by tile parity
+    // sparse: per stage, bit r set when row r of the tile is a listed, visible token
+    unsigned long long valid[kStages];
     uint64_t full[kStages], empty[kStages];
     uint64_t q_ready, s_full, s_free, p_ready, o_done, drain;
     uint64_t staged, tx_free, rx_full[2];
@@ -152,7 +154,7 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
     return __half22float2(h);
 }
 
-template <bool kSplit, bool kPaged>
+template <bool kSplit, bool kPaged, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_tc(const __grid_constant__ CUtensorMap tm_kv, const AttnParams p, const Geo g0, const Geo g1) {
     extern __shared__ uint8_t smem_raw[];
@@ -168,8 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int L = __ldg(p.seq_lens + b);
     const bool seq_ok = seq_len_ok(p, L);
+    // [t0, t1): token positions (dense) or positions in the sparse list
     int t0 = 0, t1 = 0;
-    if (seq_ok) split_range(L, p.num_splits, split, t0, t1);
+    if (seq_ok) split_range(kSparse ? p.topk : L, p.num_splits, split, t0, t1);
     const int ntiles = (t1 - t0 + kTile - 1) / kTile;
 
     if (threadIdx.x == 0) {
@@ -201,7 +204,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && kSparse) {
+        // ------------------------------------------------------------ TMA producer, sparse
+        // Tile n = listed entries e = t0 + 64 n + r.  The whole warp resolves them
+        // (lanes r and r + 32): an entry takes part if it names a token this row
+        // block's query may see, 0 <= j <= L - s_q + i (all rows of a block share
+        // i), on a page inside the pool; its cache row is gathered by tile::gather4
+        // (4 rows per copy, lanes 0-15).  Rows of entries that take no part are
+        // read from row 0 and zeroed by the score issuer before the MMAs.
+        const int W = p.d_c + p.d_rope;
+        const int iq = (rb * kRows) / p.H;
+        const int lim = L - p.s_q + iq;
+        const int *list = p.indices + ((long long)b * p.s_q + iq) * p.topk;
+        const long long seq_rows = p.seq_stride / W;  // contiguous: rows between sequences
+        int issued = 0;
+        for (int n = 0; n < ntiles; ++n) {
+            const int s = n % kStages;
+            if (n >= kStages && !warp_wait(sm, &sm.empty[s], ((n / kStages) - 1) & 1)) {
+                if (lane == 0) raise_abort<kSplit>(sm, p, peer);
+                break;
+            }
+            int rows[2];
+            bool vis[2];
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int e = t0 + n * kTile + lane + 32 * h2;
+                const int j = e < t1 ? __ldg(list + e) : -1;
+                vis[h2] = j >= 0 && j <= lim;
+                long long row = 0;
+                if (vis[h2]) {
+                    if (kPaged) {
+                        const int page = __ldg(p.block_table + (long long)b * p.max_pages + j / p.page_size);
+                        if (page >= 0 && page < p.num_pages) {
+                            row = (long long)page * p.page_size + j % p.page_size;
+                        } else {
+                            set_status(p.status, MLA_ERR_PAGE);
+                            vis[h2] = false;
+                        }
+                    } else {
+                        row = b * seq_rows + j;
+                    }
+                }
+                rows[h2] = vis[h2] ? (int)row : 0;
+            }
+            const unsigned lo = __ballot_sync(0xffffffffu, vis[0]), hi = __ballot_sync(0xffffffffu, vis[1]);
+            if (lane == 0) {
+                sm.valid[s] = (unsigned long long)hi << 32 | lo;
+                mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
+            }
+            __syncwarp();
+            // lane q (< 16) gathers rows 4q .. 4q + 3 of every box
+            int r4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int r = 4 * (lane & 15) + k;
+                const int a0 = __shfl_sync(0xffffffffu, rows[0], r & 31);
+                const int a1 = __shfl_sync(0xffffffffu, rows[1], r & 31);
+                r4[k] = r < 32 ? a0 : a1;
+            }
+            if (lane < 16)
+                for (int bx = 0; bx < g.nbox; ++bx)
+                    tma_gather4(sm.kv[s] + bx * kBoxBytes + lane * 4 * 128, &tm_kv, &sm.full[s], g.k0 + 64 * bx, r4[0],
+                                r4[1], r4[2], r4[3]);
+            issued = n + 1;
+        }
+        // every issued copy must land before this CTA may exit
+        const int first = issued > kStages ? issued - kStages : 0;
+        for (int n = first; n < issued; ++n) mbar_wait(&sm.full[n % kStages], (n / kStages) & 1);
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             // y / z coordinates of tile n's box, or false if its page is outside the pool
@@ -266,8 +335,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // tokens at or past the sequence end may hold anything (even NaN):
                 // zero them so that 0-weight products stay 0
+                if (kSparse) {
+                    // rows of entries that take no part were read from row 0: zero them
+                    const unsigned long long dead = ~sm.valid[s];
+                    if (dead) {
+                        for (int e = lane; e < kTile * 8 * g.nbox; e += 32) {
+                            const int rr = (e / 8) % kTile;
+                            if ((dead >> rr) & 1ull)
+                                reinterpret_cast<uint4 *>(sm.kv[s] + (e / (8 * kTile)) * kBoxBytes + rr * 128)[e % 8] =
+                                    make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
                 const int tok = t0 + n * kTile;
-                const int valid = min(kTile, L - tok);
+                const int valid = kSparse ? kTile : min(kTile, L - tok);
                 if (valid < kTile) {
                     for (int e = lane; e < (kTile - valid) * 8 * g.nbox; e += 32) {
                         const int bx = e / ((kTile - valid) * 8);
@@ -452,11 +535,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // mask (only tiles that reach past a limit) and half-row maximum
             const int tok0 = t0 + n * kTile;
             bool tile_ok = true;
-            if (kPaged) {
+            if (kPaged && !kSparse) {
                 const int page = __ldg(p.block_table + (long long)b * p.max_pages + tok0 / p.page_size);
                 tile_ok = page >= 0 && page < p.num_pages;  // tokens of a bad page are skipped
             }
-            const bool whole = tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q;
+            // sparse: the producer's per-row flags (listed, visible to this block's query, good page)
+            const unsigned long long vmask = kSparse ? sm.valid[n % kStages] : 0ull;
+            const bool whole = kSparse ? vmask == ~0ull
+                                       : tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q;
             float mx0 = -INFINITY, mx1 = -INFINITY;
             if (whole) {
 #pragma unroll
@@ -468,7 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kHalf; ++j) {
                     const int tok = tok0 + kHalf * hf + j;
-                    const bool vis = tile_ok && row_ok && tok < t1 && tok <= lim;
+                    const bool vis = kSparse ? ((vmask >> (kHalf * hf + j)) & 1ull) != 0
+                                             : tile_ok && row_ok && tok < t1 && tok <= lim;
                     x[j] = vis ? x[j] : -INFINITY;
                     mx0 = fmaxf(mx0, x[j]);
                 }
@@ -633,10 +720,11 @@ Geo make_geo(const AttnParams &p, int rank, bool split) {
     return g;
 }
 
-template <bool kSplit, bool kPaged>
+template <bool kSplit, bool kPaged, bool kSparse>
 cudaError_t launch_variant(const CUtensorMap &tm, const AttnParams &p, const Geo &g0, const Geo &g1, cudaStream_t st) {
     const int smem = (int)sizeof(Smem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(attn_tc<kSplit, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = attn_tc<kSplit, kPaged, kSparse>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int row_blocks = (p.s_q * p.H + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
@@ -651,7 +739,13 @@ cudaError_t launch_variant(const CUtensorMap &tm, const AttnParams &p, const Geo
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_tc<kSplit, kPaged>, tm, p, g0, g1);
+    return cudaLaunchKernelEx(&cfg, kern, tm, p, g0, g1);
+}
+
+template <bool kSplit, bool kSparse>
+cudaError_t launch_paged(const CUtensorMap &tm, const AttnParams &p, const Geo &g0, const Geo &g1, cudaStream_t st) {
+    return p.block_table ? launch_variant<kSplit, true, kSparse>(tm, p, g0, g1, st)
+                         : launch_variant<kSplit, false, kSparse>(tm, p, g0, g1, st);
 }
 
 }  // namespace
@@ -659,10 +753,19 @@ cudaError_t launch_variant(const CUtensorMap &tm, const AttnParams &p, const Geo
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
     const int W = p.d_c + p.d_rope;
     const bool split = p.d_c > 256;
+    const bool sparse = p.indices != nullptr;
     const Geo g0 = make_geo(p, 0, split), g1 = make_geo(p, 1, split);
     if (g0.nbox > kMaxBoxes || g1.nbox > kMaxBoxes || g0.kw % 16 || g1.kw % 16) return cudaErrorNotSupported;
     CUtensorMap tm;
-    if (p.block_table) {
+    if (sparse) {
+        // every cache row of the contiguous cache or the pool, gathered one row per entry
+        const uint64_t rows = p.block_table ? (uint64_t)p.num_pages * p.page_size
+                                            : (uint64_t)p.B * (uint64_t)(p.seq_stride / W);
+        uint64_t dims[2] = {(uint64_t)W, rows};
+        uint64_t strides[1] = {(uint64_t)W * 2};
+        uint32_t box[2] = {64, 1};
+        if (!encode_bf16_sw128(&tm, p.kv, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    } else if (p.block_table) {
         uint64_t dims[2] = {(uint64_t)W, (uint64_t)p.num_pages * p.page_size};
         uint64_t strides[1] = {(uint64_t)W * 2};
         uint32_t box[2] = {64, kTile};
@@ -674,8 +777,8 @@ cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
         if (!encode_bf16_sw128(&tm, p.kv, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }
     cudaError_t e;
-    if (split) e = p.block_table ? launch_variant<true, true>(tm, p, g0, g1, st) : launch_variant<true, false>(tm, p, g0, g1, st);
-    else e = p.block_table ? launch_variant<false, true>(tm, p, g0, g1, st) : launch_variant<false, false>(tm, p, g0, g1, st);
+    if (split) e = sparse ? launch_paged<true, true>(tm, p, g0, g1, st) : launch_paged<true, false>(tm, p, g0, g1, st);
+    else e = sparse ? launch_paged<false, true>(tm, p, g0, g1, st) : launch_paged<false, false>(tm, p, g0, g1, st);
     if (e != cudaSuccess || p.num_splits == 1) return e;
     return launch_attn_combine(p, st);
 }

@@ -26,6 +26,8 @@ struct AttnParams {
     float *part_acc;              // [B][splits][s_q*H][d_c] (num_splits > 1)
     float *part_ml;               // [B][splits][s_q*H][2 CTA halves][2]   (m, l)
     int *status;                  // device status word
+    const int *indices;           // sparse: [B][s_q][topk] token positions (NULL => dense)
+    int topk;
 };
 
 // Record the first device-side error; later ones keep the first.

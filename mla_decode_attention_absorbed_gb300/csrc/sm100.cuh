@@ -180,6 +180,16 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m, uin
 }
 
 // Prefetch a tensor box into L2 only (no shared memory, no barrier).
+// Four rows (row0..row3) of a 2-D tensor, columns [x, x + box width), into
+// consecutive box-width rows at dst (tile::gather4; the map's box is one row).
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *m, uint64_t *bar, int x, int row0, int row1,
+                                            int row2, int row3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(row0), "r"(row1), "r"(row2), "r"(row3), "r"(smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *m, int x, int y) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
                  "r"(x), "r"(y)

@@ -38,7 +38,7 @@ class Cache(ctypes.Structure):
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_workspace_size",
            "mla_decode_num_splits", "mla_decode_attn", "mla_out_proj", "mla_naive_workspace_size",
            "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc", "mla_cache_append_workspace_size",
-           "mla_cache_append")
+           "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse")
 
 
 def lib_path() -> str:
@@ -73,6 +73,10 @@ def load(path: str | None = None):
     lib.mla_naive_workspace_size.restype = SZ
     lib.mla_naive_decode.argtypes = [pd, P, P, pc, P, P, P, P, P, SZ, P]
     lib.mla_naive_decode.restype = I
+    lib.mla_decode_sparse_workspace_size.argtypes = [pd, pc, I, I]
+    lib.mla_decode_sparse_workspace_size.restype = SZ
+    lib.mla_decode_attn_sparse.argtypes = [pd, P, pc, P, I, P, P, P, SZ, I, P]
+    lib.mla_decode_attn_sparse.restype = I
     lib.mla_cache_append_workspace_size.argtypes = [pd, I]
     lib.mla_cache_append_workspace_size.restype = SZ
     lib.mla_cache_append.argtypes = [pd, I, P, P, P, pc, P, SZ, P]
@@ -200,6 +204,33 @@ def out_proj(prob: Problem, o_lat, w_uv, out=None, stream=None):
     return out
 
 
+def decode_sparse_workspace_size(prob: Problem, cache: Cache, topk: int, num_splits: int = 0) -> int:
+    d = prob.dims()
+    n = load().mla_decode_sparse_workspace_size(ctypes.byref(d), ctypes.byref(cache), int(topk), int(num_splits))
+    if n == 0:
+        raise ValueError("mla_decode_sparse_workspace_size rejected the arguments")
+    return int(n)
+
+
+def decode_attn_sparse(prob: Problem, q_cat, cache: Cache, indices, num_splits: int = 0, o_lat=None, lse=None,
+                       workspace=None, stream=None):
+    """mla_decode_attn_sparse: attention over the listed tokens (indices int32 [B, s_q, topk])."""
+    lib = load()
+    dev = q_cat.device
+    topk = int(indices.shape[-1])
+    if o_lat is None:
+        o_lat = torch.empty(prob.B, prob.s_q, prob.H, prob.d_c, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(prob.B, prob.s_q, prob.H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(decode_sparse_workspace_size(prob, cache, topk, num_splits), dev)
+    d = prob.dims()
+    _check(lib.mla_decode_attn_sparse(ctypes.byref(d), _ptr(q_cat), ctypes.byref(cache), _ptr(indices), topk,
+                                      _ptr(o_lat), _ptr(lse), _ptr(workspace), workspace.numel(), int(num_splits),
+                                      _stream(stream)), "mla_decode_attn_sparse")
+    return o_lat, lse, workspace
+
+
 def cache_append_workspace_size(prob: Problem, d_model: int) -> int:
     d = prob.dims()
     n = load().mla_cache_append_workspace_size(ctypes.byref(d), int(d_model))
@@ -217,7 +248,7 @@ def cache_append(prob: Problem, x, w_dkv, k_rope, cache: Cache, workspace=None, 
     d = prob.dims()
     _check(lib.mla_cache_append(ctypes.byref(d), int(x.shape[-1]), _ptr(x), _ptr(w_dkv), _ptr(k_rope),
                                 ctypes.byref(cache), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "mla_cache_append")
+           "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse")
     return workspace
 
 

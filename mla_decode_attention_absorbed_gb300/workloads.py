@@ -69,6 +69,8 @@ CONFIGS = {
     "long": MLAConfig("long", B=16, s_q=1, T=32768, **_DSV3),
     # speculative verify: 3 drafts + bonus, causal among the 4
     "spec": MLAConfig("spec", B=64, s_q=4, T=8192, **_DSV3),
+    # sparse top-k decode: long histories, k = 2048 listed tokens per query token
+    "sparse": MLAConfig("sparse", B=64, s_q=1, T=32768, **_DSV3),
     # ragged lengths over a shuffled paged pool
     "ragged_paged": MLAConfig("ragged_paged", B=128, s_q=2, len_lo=512, len_hi=16384, paged=True,
                               page_size=64, **_DSV3),
