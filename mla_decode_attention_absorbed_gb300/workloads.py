@@ -138,6 +138,18 @@ def make_inputs(cfg: MLAConfig, seq_lens=None) -> dict:
                 T_max=(kv.shape[1] if not cfg.paged else block_table.shape[1] * cfg.page_size))
 
 
+# Scale of the FP8 latent-cache workloads: codes hold value / 2^-4, so the
+# N(0, 1) values of the drawn cache use E4M3's range (max 448) without clipping.
+KV_FP8_SCALE = 1.0 / 16.0
+
+
+def to_fp8_cache(kv: torch.Tensor, kv_scale: float = KV_FP8_SCALE) -> torch.Tensor:
+    """E4M3 codes (uint8, same shape) of a drawn bf16 cache, for the FP8-cache
+    workloads: each value divided by ``kv_scale`` and cast by torch's
+    float8_e4m3fn conversion (round to nearest even); NaN canaries stay NaN."""
+    return (kv.to(torch.float32) / kv_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
 def make_append_inputs(cfg: MLAConfig, d_model: int, seed: int = 7) -> dict:
     """Inputs of the cache-append step (latent down-projection of the new tokens).
 

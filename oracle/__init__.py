@@ -9,7 +9,8 @@ none of the method's arithmetic.
 The numerics live in ``mla_oracle.c`` (plain fp64 loops, OpenMP over output
 rows), compiled on first use with the host C compiler; ``counts.py`` holds the
 closed-form FLOP / byte counters the pages print.  Inputs are the exact bf16
-tensors handed to the GPU (bit patterns, widened to fp64 inside the C code);
+tensors handed to the GPU (bit patterns, widened to fp64 inside the C code) or,
+for an FP8 latent cache, its E4M3 codes (uint8) and the cache's one scale;
 activations returned here are float64 CPU tensors.
 """
 from __future__ import annotations
@@ -58,7 +59,7 @@ class _Cache(ctypes.Structure):
     _fields_ = [("kv", ctypes.c_void_p), ("seq_stride", ctypes.c_longlong),
                 ("block_table", ctypes.c_void_p), ("max_pages", ctypes.c_int),
                 ("page_size", ctypes.c_int), ("capacity", ctypes.c_longlong),
-                ("seq_lens", ctypes.c_void_p)]
+                ("seq_lens", ctypes.c_void_p), ("elem", ctypes.c_int), ("kv_scale", ctypes.c_double)]
 
 
 def _load():
@@ -68,6 +69,8 @@ def _load():
             lib = ctypes.CDLL(build())
             P, LL = ctypes.c_void_p, ctypes.c_longlong
             lib.orc_threads.restype = ctypes.c_int
+            lib.orc_e4m3_to_f64.restype = ctypes.c_double
+            lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
             lib.orc_absorb_q.argtypes = [ctypes.POINTER(_Dims), P, P, P, P]
             lib.orc_attend.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache), P, LL, P, P]
             lib.orc_attend_partial.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache),
@@ -118,10 +121,18 @@ class _CacheArgs:
 
     Contiguous cache: ``kv`` is [B, T_max, d_c + d_rope] (any strides; copied
     contiguous here).  Paged cache: ``kv`` is the pool [P, page_size, d_c + d_rope]
-    and ``block_table`` is [B, max_pages]."""
+    and ``block_table`` is [B, max_pages].  ``kv`` is bf16, or uint8 /
+    float8_e4m3fn E4M3 codes together with ``kv_scale`` (value = kv_scale * code)."""
 
-    def __init__(self, d, kv, seq_lens, block_table=None, page_size=64):
-        self.kv = _bits(kv)
+    def __init__(self, d, kv, seq_lens, block_table=None, page_size=64, kv_scale=None):
+        if kv.dtype in (torch.uint8, torch.float8_e4m3fn):
+            if kv_scale is None:
+                raise ValueError("an FP8 cache needs its kv_scale")
+            self.kv = kv.detach().to("cpu").contiguous().view(torch.uint8)
+            elem, scale = 1, float(kv_scale)
+        else:
+            self.kv = _bits(kv)
+            elem, scale = 0, 1.0
         self.seq_lens = _i32(seq_lens)
         self.block_table = _i32(block_table) if block_table is not None else None
         W = d.d_c + d.d_rope
@@ -130,11 +141,11 @@ class _CacheArgs:
         if self.block_table is None:
             t_max = int(kv.shape[1])
             self.c = _Cache(_ptr(self.kv).value, t_max * W, None, 0, int(page_size), t_max,
-                            _ptr(self.seq_lens).value)
+                            _ptr(self.seq_lens).value, elem, scale)
         else:
             max_pages = int(self.block_table.shape[1])
             self.c = _Cache(_ptr(self.kv).value, 0, _ptr(self.block_table).value, max_pages,
-                            int(page_size), max_pages * int(page_size), _ptr(self.seq_lens).value)
+                            int(page_size), max_pages * int(page_size), _ptr(self.seq_lens).value, elem, scale)
 
 
 def _rows_arg(rows):
@@ -154,14 +165,19 @@ def absorb_q(d, q_nope, q_rope, w_uk) -> torch.Tensor:
     return out
 
 
-def attend(d, q_cat, kv, seq_lens, block_table=None, page_size=64, rows=None):
+def e4m3_to_f64(code: int) -> float:
+    """Value of one OCP FP8 E4M3 code (see orc_e4m3_to_f64)."""
+    return float(_load().orc_e4m3_to_f64(int(code) & 0xFF))
+
+
+def attend(d, q_cat, kv, seq_lens, block_table=None, page_size=64, rows=None, kv_scale=None):
     """(o_lat [B, s_q, H, d_c], lse [B, s_q, H]) float64 from a float64-widened q_cat.
 
     ``rows`` optionally lists flat row indices (b*s_q + i)*H + h to compute; other
-    rows are returned as NaN."""
+    rows are returned as NaN.  An FP8 cache (uint8 codes) needs ``kv_scale``."""
     lib = _load()
     q = _f64(q_cat)
-    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size, kv_scale)
     o = torch.full((d.B, d.s_q, d.H, d.d_c), float("nan"), dtype=torch.float64)
     lse = torch.full((d.B, d.s_q, d.H), float("nan"), dtype=torch.float64)
     r, n = _rows_arg(rows)
@@ -169,14 +185,14 @@ def attend(d, q_cat, kv, seq_lens, block_table=None, page_size=64, rows=None):
     return o, lse
 
 
-def attend_sparse(d, q_cat, kv, seq_lens, indices, block_table=None, page_size=64, rows=None):
+def attend_sparse(d, q_cat, kv, seq_lens, indices, block_table=None, page_size=64, rows=None, kv_scale=None):
     """Sparse top-k attention: (o_lat, lse) float64 over the listed tokens only.
 
     ``indices`` [B, s_q, topk] int32: token positions per query token, shared by
     the heads; entries that do not name a visible token (e.g. -1) take no part."""
     lib = _load()
     q = _f64(q_cat)
-    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size, kv_scale)
     idx = _i32(indices)
     topk = int(idx.shape[-1])
     o = torch.full((d.B, d.s_q, d.H, d.d_c), float("nan"), dtype=torch.float64)
@@ -187,11 +203,11 @@ def attend_sparse(d, q_cat, kv, seq_lens, indices, block_table=None, page_size=6
     return o, lse
 
 
-def attend_partial(d, q_cat, kv, seq_lens, row, j0, j1, block_table=None, page_size=64):
+def attend_partial(d, q_cat, kv, seq_lens, row, j0, j1, block_table=None, page_size=64, kv_scale=None):
     """Unnormalised partial (m, l, acc[d_c]) of one flat row over tokens [j0, j1)."""
     lib = _load()
     q = _f64(q_cat)
-    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size)
+    ca = _CacheArgs(d, kv, seq_lens, block_table, page_size, kv_scale)
     m = torch.zeros(1, dtype=torch.float64)
     l = torch.zeros(1, dtype=torch.float64)
     acc = torch.zeros(d.d_c, dtype=torch.float64)
@@ -282,13 +298,14 @@ def naive(d, q_nope, q_rope, kv, seq_lens, w_uk, w_uv, block_table=None, page_si
     return out, lse
 
 
-def decode(d, q_nope, q_rope, kv, seq_lens, w_uk, w_uv, block_table=None, page_size=64, rows=None):
+def decode(d, q_nope, q_rope, kv, seq_lens, w_uk, w_uv, block_table=None, page_size=64, rows=None,
+           kv_scale=None):
     """Absorbed decode end to end in fp64: dict(q_cat, o_lat, lse, out).
 
     With ``rows`` the attention runs on those rows only; out is then valid on
     those rows only."""
     q_cat = absorb_q(d, q_nope, q_rope, w_uk)
-    o_lat, lse = attend(d, q_cat, kv, seq_lens, block_table, page_size, rows)
+    o_lat, lse = attend(d, q_cat, kv, seq_lens, block_table, page_size, rows, kv_scale)
     out = out_proj(d, torch.nan_to_num(o_lat, nan=0.0) if rows is not None else o_lat, w_uv)
     if rows is not None:
         keep = torch.zeros(d.B * d.s_q * d.H, dtype=torch.bool)

@@ -25,7 +25,8 @@
  *             "The naive form, written out", "The identity", "The absorbed form".
  *  [intens]   "Decode attention intensity is fixed at the query-to-KV head
  *             ratio..." -- "A strong answer" (576-wide latent: 512 c_kv + 64 RoPE
- *             key per token, shared by all heads).
+ *             key per token, shared by all heads; with an FP8 latent the same
+ *             576 values take one byte each).
  *
  * Readings where the pages are silent (each also listed in the design doc):
  *  - the cached token row is [c_kv (d_c) | k_rope (d_rope)], contiguous;
@@ -34,7 +35,10 @@
  *    (0-based) sits at position L - s_q + i and sees cached tokens j <= L - s_q + i;
  *  - lse is the natural-log log-sum-exp of the *scaled* scores;
  *  - an invalid length (L < s_q, or L beyond the cache) yields NaN rows here:
- *    the oracle is never asked to agree with the GPU on invalid input.
+ *    the oracle is never asked to agree with the GPU on invalid input;
+ *  - an FP8 latent cache holds OCP FP8 E4M3 codes (1 sign, 4 exponent bits with
+ *    bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN) and one fp32
+ *    scale for the whole cache: a cached value is kv_scale * code.
  */
 #include <math.h>
 #include <stdint.h>
@@ -50,13 +54,15 @@ typedef struct {
 } orc_dims;
 
 typedef struct {
-    const uint16_t *kv;          /* bf16 bits; contiguous [B][seq_stride] or pool [P][page][W] */
+    const void *kv;              /* bf16 bits or e4m3 codes; contiguous [B][seq_stride] or pool [P][page][W] */
     long long seq_stride;        /* contiguous layout: elements between two sequences */
     const int32_t *block_table;  /* NULL => contiguous; else [B][max_pages] page ids */
     int max_pages;
     int page_size;
     long long capacity;          /* tokens a sequence may hold (contiguous: T_max) */
     const int32_t *seq_lens;     /* [B] */
+    int elem;                    /* 0: bf16 elements, 1: FP8 E4M3 codes */
+    double kv_scale;             /* elem 1: a cached value is kv_scale * code */
 } orc_cache;
 
 /* bf16 is the upper half of an IEEE binary32; widening is exact. */
@@ -66,6 +72,23 @@ static double bf16_to_f64(uint16_t bits)
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* OCP FP8 E4M3: (-1)^s * 2^(e-7) * (1 + m/8) for e > 0, (-1)^s * 2^-6 * (m/8)
+ * for e = 0 (subnormal); e = 15 with m = 7 is NaN, there is no infinity. */
+double orc_e4m3_to_f64(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* Element k of a cached row (bf16 widened, or the scaled FP8 value). */
+static double row_elem(const orc_cache *c, const void *row, long long k)
+{
+    if (c->elem == 1) return c->kv_scale * orc_e4m3_to_f64(((const uint8_t *)row)[k]);
+    return bf16_to_f64(((const uint16_t *)row)[k]);
 }
 
 int orc_threads(void)
@@ -79,13 +102,18 @@ int orc_threads(void)
 
 /* Token j of sequence b: contiguous rows, or page block_table[b][j / page]
  * row j % page of the shared pool. */
-static const uint16_t *token_row(const orc_dims *d, const orc_cache *c, int b, long long j)
+static const void *token_row(const orc_dims *d, const orc_cache *c, int b, long long j)
 {
     long long w = (long long)d->d_c + d->d_rope;
-    if (c->block_table == NULL)
-        return c->kv + (long long)b * c->seq_stride + j * w;
-    long long page = c->block_table[(long long)b * c->max_pages + j / c->page_size];
-    return c->kv + (page * c->page_size + j % c->page_size) * w;
+    long long esize = c->elem == 1 ? 1 : 2;
+    long long at;
+    if (c->block_table == NULL) {
+        at = (long long)b * c->seq_stride + j * w;
+    } else {
+        long long page = c->block_table[(long long)b * c->max_pages + j / c->page_size];
+        at = (page * c->page_size + j % c->page_size) * w;
+    }
+    return (const uint8_t *)c->kv + at * esize;
 }
 
 /* Absorb W_UK into the query ([MLA-dim] "MLA Decode", decode score order;
@@ -154,10 +182,10 @@ static void attend_row(const orc_dims *d, const double *q_cat, const orc_cache *
     long long n_vis = L - d->s_q + i + 1;
     double m = -INFINITY;
     for (long long j = 0; j < n_vis; ++j) {
-        const uint16_t *t = token_row(d, c, b, j);
+        const void *t = token_row(d, c, b, j);
         double dot = 0.0;
         for (long long k = 0; k < wq; ++k)
-            dot += q[k] * bf16_to_f64(t[k]);
+            dot += q[k] * row_elem(c, t, k);
         scores[j] = d->scale * dot;
         if (scores[j] > m) m = scores[j];
     }
@@ -168,9 +196,9 @@ static void attend_row(const orc_dims *d, const double *q_cat, const orc_cache *
     for (int k = 0; k < d->d_c; ++k) o[k] = 0.0;
     for (long long j = 0; j < n_vis; ++j) {
         double p = exp(scores[j] - l);
-        const uint16_t *t = token_row(d, c, b, j);
+        const void *t = token_row(d, c, b, j);
         for (int k = 0; k < d->d_c; ++k)
-            o[k] += p * bf16_to_f64(t[k]);
+            o[k] += p * row_elem(c, t, k);
     }
     lse[r] = l;
 }
@@ -232,10 +260,10 @@ static void attend_row_sparse(const orc_dims *d, const double *q_cat, const orc_
         long long j = list[e];
         scores[e] = -INFINITY;
         if (j < 0 || j > lim) continue;
-        const uint16_t *t = token_row(d, c, b, j);
+        const void *t = token_row(d, c, b, j);
         double dot = 0.0;
         for (long long k = 0; k < wq; ++k)
-            dot += q[k] * bf16_to_f64(t[k]);
+            dot += q[k] * row_elem(c, t, k);
         scores[e] = d->scale * dot;
         if (scores[e] > m) m = scores[e];
     }
@@ -251,9 +279,9 @@ static void attend_row_sparse(const orc_dims *d, const double *q_cat, const orc_
     for (int e = 0; e < topk; ++e) {
         if (scores[e] == -INFINITY) continue;
         double p = exp(scores[e] - l);
-        const uint16_t *t = token_row(d, c, b, list[e]);
+        const void *t = token_row(d, c, b, list[e]);
         for (int k = 0; k < d->d_c; ++k)
-            o[k] += p * bf16_to_f64(t[k]);
+            o[k] += p * row_elem(c, t, k);
     }
     lse[r] = l;
 }
@@ -291,21 +319,21 @@ void orc_attend_partial(const orc_dims *d, const double *q_cat, const orc_cache 
     double m = -INFINITY;
     for (int k = 0; k < d->d_c; ++k) acc[k] = 0.0;
     for (long long j = j0; j < j1; ++j) {
-        const uint16_t *t = token_row(d, c, b, j);
+        const void *t = token_row(d, c, b, j);
         double dot = 0.0;
-        for (long long k = 0; k < wq; ++k) dot += q[k] * bf16_to_f64(t[k]);
+        for (long long k = 0; k < wq; ++k) dot += q[k] * row_elem(c, t, k);
         double s = d->scale * dot;
         if (s > m) m = s;
     }
     double l = 0.0;
     if (m != -INFINITY) {
         for (long long j = j0; j < j1; ++j) {
-            const uint16_t *t = token_row(d, c, b, j);
+            const void *t = token_row(d, c, b, j);
             double dot = 0.0;
-            for (long long k = 0; k < wq; ++k) dot += q[k] * bf16_to_f64(t[k]);
+            for (long long k = 0; k < wq; ++k) dot += q[k] * row_elem(c, t, k);
             double e = exp(d->scale * dot - m);
             l += e;
-            for (int k = 0; k < d->d_c; ++k) acc[k] += e * bf16_to_f64(t[k]);
+            for (int k = 0; k < d->d_c; ++k) acc[k] += e * row_elem(c, t, k);
         }
     }
     *m_out = m;
@@ -416,11 +444,11 @@ void orc_naive(const orc_dims *d, const uint16_t *q_nope, const uint16_t *q_rope
             long long L = c->seq_lens[b];
             long long n_vis = L - d->s_q + i + 1;
             for (long long j = 0; j < n_vis; ++j) {
-                const uint16_t *tok = token_row(d, c, b, j);
+                const void *tok = token_row(d, c, b, j);
                 for (int n = 0; n < d->d_nope; ++n) K[j * d->d_nope + n] = 0.0;
                 for (int v = 0; v < d->d_v; ++v) V[j * d->d_v + v] = 0.0;
                 for (int cc = 0; cc < d->d_c; ++cc) {
-                    double x = bf16_to_f64(tok[cc]);
+                    double x = row_elem(c, tok, cc);
                     const uint16_t *wk = w_uk + ((long long)h * d->d_c + cc) * d->d_nope;
                     const uint16_t *wv = w_uv + ((long long)h * d->d_c + cc) * d->d_v;
                     for (int n = 0; n < d->d_nope; ++n) K[j * d->d_nope + n] += x * bf16_to_f64(wk[n]);
@@ -431,10 +459,10 @@ void orc_naive(const orc_dims *d, const uint16_t *q_nope, const uint16_t *q_rope
             const uint16_t *qr = q_rope + r * d->d_rope;
             double m = -INFINITY;
             for (long long j = 0; j < n_vis; ++j) {
-                const uint16_t *tok = token_row(d, c, b, j);
+                const void *tok = token_row(d, c, b, j);
                 double dot = 0.0;
                 for (int n = 0; n < d->d_nope; ++n) dot += bf16_to_f64(qn[n]) * K[j * d->d_nope + n];
-                for (int k = 0; k < d->d_rope; ++k) dot += bf16_to_f64(qr[k]) * bf16_to_f64(tok[d->d_c + k]);
+                for (int k = 0; k < d->d_rope; ++k) dot += bf16_to_f64(qr[k]) * row_elem(c, tok, d->d_c + k);
                 scores[j] = d->scale * dot;
                 if (scores[j] > m) m = scores[j];
             }

@@ -515,3 +515,73 @@ def test_sparse_no_visible_entry_gives_zero_and_minus_inf():
     idx = torch.full((cfg.B, 1, 8), -1, dtype=torch.int32)
     o, lse = oracle.attend_sparse(cfg, q, inp["kv"], inp["seq_lens"], idx)
     assert torch.equal(o, torch.zeros_like(o)) and bool(torch.isneginf(lse).all())
+
+
+# ------------------------------------------------------------------ FP8 (E4M3) latent cache
+def test_e4m3_decode_matches_library_for_every_code():
+    """The oracle's E4M3 decoder against torch's float8_e4m3fn for all 256 codes,
+    plus the format's landmarks (1, max 448, smallest subnormal 2^-9, NaN)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    mine = torch.tensor([oracle.e4m3_to_f64(c) for c in range(256)], dtype=torch.float64)
+    nan = torch.isnan(lib)
+    assert torch.equal(nan, torch.isnan(mine)) and int(nan.sum()) == 2  # 0x7F and 0xFF
+    assert torch.equal(lib[~nan], mine[~nan])
+    assert oracle.e4m3_to_f64(0x38) == 1.0 and oracle.e4m3_to_f64(0x7E) == 448.0
+    assert oracle.e4m3_to_f64(0x01) == 2.0 ** -9 and oracle.e4m3_to_f64(0x08) == 2.0 ** -6
+    assert oracle.e4m3_to_f64(0xB8) == -1.0
+
+
+def _fp8_case(paged=False, s_q=2, kv_scale=1.0 / 16.0):
+    from mla_decode_attention_absorbed_gb300.workloads import to_fp8_cache
+    cfg = MLAConfig("fp8_pin", B=3, H=4, d_c=64, d_rope=16, d_nope=32, d_v=32, s_q=s_q,
+                    len_lo=20, len_hi=90, paged=paged, seed=31, canary=True)
+    inp = make_inputs(cfg)
+    codes = to_fp8_cache(inp["kv"], kv_scale)
+    q_cat = oracle.absorb_q(cfg, inp["q_nope"], inp["q_rope"], inp["w_uk"]).to(torch.bfloat16)
+    return cfg, inp, codes, q_cat
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_fp8_cache_equals_bf16_cache_of_its_values(paged):
+    """With a power-of-two scale every kv_scale * code is a bf16 number: attention
+    over the FP8 cache must equal, bit for bit, attention over that bf16 cache."""
+    cfg, inp, codes, q = _fp8_case(paged)
+    deq = (codes.view(torch.float8_e4m3fn).to(torch.float32) / 16.0).to(torch.bfloat16)
+    o8, l8 = oracle.attend(cfg, q, codes, inp["seq_lens"], inp["block_table"], cfg.page_size, kv_scale=1.0 / 16.0)
+    ob, lb = oracle.attend(cfg, q, deq, inp["seq_lens"], inp["block_table"], cfg.page_size)
+    assert torch.equal(o8, ob) and torch.equal(l8, lb)
+
+
+def test_fp8_cache_scale_enters_scores_and_values():
+    """A non-power-of-two scale against SDPA on the library-decoded values: the
+    scale multiplies both the keys (scores) and the values (latent sum)."""
+    s = 0.0371
+    cfg, inp, codes, q = _fp8_case(kv_scale=s)
+    o8, l8 = oracle.attend(cfg, q, codes, inp["seq_lens"], kv_scale=s)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64) * s
+    for b in range(cfg.B):
+        L = int(inp["seq_lens"][b])
+        rows = vals[b, :L]
+        qq = f64(q[b]).transpose(0, 1)
+        mask = torch.tensor([[j <= L - cfg.s_q + i for j in range(L)] for i in range(cfg.s_q)])
+        o = F.scaled_dot_product_attention(qq, rows.expand(cfg.H, L, cfg.W), rows[:, :cfg.d_c].expand(cfg.H, L, cfg.d_c),
+                                           attn_mask=mask, scale=cfg.scale)
+        torch.testing.assert_close(o8[b], o.transpose(0, 1), rtol=1e-11, atol=1e-12)
+
+
+def test_fp8_sparse_full_list_is_dense():
+    cfg, inp, codes, q = _fp8_case(paged=True)
+    idx = _full_lists(cfg, inp["seq_lens"], extra=3)
+    o_s, l_s = oracle.attend_sparse(cfg, q, codes, inp["seq_lens"], idx, inp["block_table"], cfg.page_size,
+                                    kv_scale=1.0 / 16.0)
+    o_d, l_d = oracle.attend(cfg, q, codes, inp["seq_lens"], inp["block_table"], cfg.page_size, kv_scale=1.0 / 16.0)
+    assert torch.allclose(o_s, o_d, rtol=0, atol=1e-12) and torch.allclose(l_s, l_d, rtol=0, atol=1e-12)
+
+
+def test_fp8_canaries_stay_unread():
+    """NaN codes sit in every row past a sequence's length; no output may be NaN."""
+    cfg, inp, codes, q = _fp8_case()
+    assert bool((codes == 0x7F).any())
+    o8, l8 = oracle.attend(cfg, q, codes, inp["seq_lens"], kv_scale=1.0 / 16.0)
+    assert not torch.isnan(o8).any() and not torch.isnan(l8).any()
