@@ -393,11 +393,16 @@ def _timed_steps(step, K, flush, stream, dev):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+TOPK = 2048  # DeepSeek-V3.2's index_topk
+
+
 def main_op(args):
     """One JSON line for a non-headline row of the path, same contract as the decode line."""
     rank, world, local = dist_env()
     active = init_dist(world, args.backend)
-    cfg = CONFIGS[args.config]
+    cfg = CONFIGS["sparse" if args.op == "sparse" and args.config == DEFAULT_CONFIG else args.config]
+    if args.op == "sparse":
+        return main_sparse(args, cfg, rank, world, local, active)
     from mla_decode_attention_absorbed_gb300 import mla
     from mla_decode_attention_absorbed_gb300.workloads import make_append_inputs
 
@@ -527,6 +532,169 @@ def main_op(args):
     print(json.dumps(line))
 
 
+def cpu_baseline_sparse(cfg, inp, idx, per_pair_flops, budget_s: float = 12.0):
+    """The oracle as it stands: absorb, sparse attention and out_proj in fp64 on
+    whole sequences of the same workload until about ``budget_s`` of host time."""
+    import oracle
+    from oracle import counts
+    done, t_used, n = 0, 0.0, 0
+    sub = cfg.with_(B=1)
+    for b in range(cfg.B):
+        bt = None if inp["block_table"] is None else inp["block_table"][b:b + 1]
+        kv = inp["kv"][b:b + 1] if bt is None else inp["kv"]
+        L = inp["seq_lens"][b:b + 1]
+        t0 = time.perf_counter()
+        q_cat = oracle.absorb_q(sub, inp["q_nope"][b:b + 1], inp["q_rope"][b:b + 1], inp["w_uk"])
+        o_lat, _ = oracle.attend_sparse(sub, q_cat, kv, L, idx[b:b + 1], bt, cfg.page_size)
+        oracle.out_proj(sub, o_lat, inp["w_uv"])
+        t_used += time.perf_counter() - t0
+        lim = int(L[0]) - cfg.s_q + torch.arange(cfg.s_q).view(-1, 1)
+        pairs = int(((idx[b] >= 0) & (idx[b] <= lim)).sum())
+        done += (pairs * per_pair_flops + counts.absorb_flops(1, cfg.s_q, cfg.H, cfg.d_nope, cfg.d_c)
+                 + counts.out_proj_flops(1, cfg.s_q, cfg.H, cfg.d_c, cfg.d_v))
+        n += 1
+        if t_used >= budget_s:
+            break
+    return {"value": done / t_used / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n} of {cfg.B} sequences of the sparse top-{TOPK} step (fp64), {t_used:.1f} s"}
+
+
+def main_sparse(args, cfg, rank, world, local, active):
+    """The decode step with the attention over k = TOPK listed tokens per query token."""
+    from mla_decode_attention_absorbed_gb300 import mla
+    from mla_decode_attention_absorbed_gb300.workloads import make_sparse_indices
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    mla.load()
+    c = cfg.with_(seed=replica_seed(cfg.seed, rank))
+    inp = make_inputs(c)
+    idx = make_sparse_indices(c, inp["seq_lens"], TOPK)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    d_idx = idx.to(dev)
+    prob = mla.Problem.of(c)
+    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size)
+    q_cat = torch.empty(c.B, c.s_q, c.H, c.W, dtype=torch.bfloat16, device=dev)
+    o_lat = torch.empty(c.B, c.s_q, c.H, c.d_c, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(c.B, c.s_q, c.H, dtype=torch.float32, device=dev)
+    out = torch.empty(c.B, c.s_q, c.H, c.d_v, dtype=torch.bfloat16, device=dev)
+    ws = mla.alloc_workspace(mla.decode_sparse_workspace_size(prob, cache, TOPK, args.splits), dev)
+    # algorithmic work: the visible listed pairs, each listed cache row read once per query token
+    n_pairs = int(((idx >= 0) & (idx <= (inp["seq_lens"].view(-1, 1, 1) - c.s_q
+                                        + torch.arange(c.s_q).view(1, -1, 1)))).sum())
+    per_pair_flops = 2 * c.H * (c.W + c.d_c)
+    attn_flops = n_pairs * per_pair_flops
+    attn_bytes = n_pairs * c.W * 2 + q_cat.numel() * 2 + o_lat.numel() * 2 + lse.numel() * 4 + idx.numel() * 4
+    proj_flops = 2 * c.B * c.s_q * c.H * c.d_nope * c.d_c + 2 * c.B * c.s_q * c.H * c.d_c * c.d_v
+    step_flops = attn_flops + proj_flops
+
+    def absorb():
+        mla.absorb_q(prob, d["q_nope"], d["q_rope"], d["w_uk"], q_cat=q_cat)
+
+    def attend():
+        mla.decode_attn_sparse(prob, q_cat, cache, d_idx, num_splits=args.splits, o_lat=o_lat, lse=lse,
+                               workspace=ws)
+
+    def project():
+        mla.out_proj(prob, o_lat, d["w_uv"], out=out)
+
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        absorb(); attend(); project()
+    torch.cuda.synchronize(dev)
+    st = mla.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier(active)
+    torch.cuda.synchronize(dev)
+    for k in range(K):
+        flush.zero_()
+        ev[k][0].record(stream)
+        absorb()
+        ev_a[k][0].record(stream)
+        attend()
+        ev_a[k][1].record(stream)
+        project()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(active)
+    clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = sum(a.elapsed_time(b) for a, b in ev_a) / K
+    ms = reduce_max(sum(step_ms) / K, active, "cuda" if active and args.backend == "nccl" else "cpu")
+    # end to end: pinned q_nope / q_rope / index lists in, out back, every step
+    h_qn, h_qr, h_idx = inp["q_nope"].pin_memory(), inp["q_rope"].pin_memory(), idx.pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_steps = max(3, min(K, 50))
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        d["q_nope"].copy_(h_qn, non_blocking=True)
+        d["q_rope"].copy_(h_qr, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        absorb(); attend(); project()
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active, "cuda" if active and args.backend == "nccl" else "cpu")
+    if rank != 0:
+        return
+    pk = peaks()
+    attn_s = attn_ms * 1e-3
+    tensor_bound = attn_flops / (pk["bf16_tflops"] * 1e12) > attn_bytes / (pk["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        ach = attn_flops / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / pk["bf16_tflops"]}
+    else:
+        ach = attn_bytes / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
+    roof.update({"traffic": None, "kernel": "mla_decode_attn_sparse (gathered top-k attention)",
+                 "peak_source": pk["source"] + (" burst bf16" if tensor_bound else " HBM copy"),
+                 "roofline_time_us": max(attn_flops / (pk["bf16_tflops"] * 1e12),
+                                         attn_bytes / (pk["hbm_gbs"] * 1e9)) * 1e6,
+                 "kernel_us": attn_ms * 1e3})
+    cpu = None if args.no_cpu_baseline else cpu_baseline_sparse(c, inp, idx, per_pair_flops)
+    line = {
+        "metric": f"MLA sparse top-{TOPK} decode TFLOP/s (H=128, d_c=512+64, 1xGB300)",
+        "value": step_flops * world / (ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights, uniform random top-k lists)",
+        "config": {"workload": f"{workload_name(c)}, top-{TOPK} lists", "num_splits": args.splits,
+                   "l2": "L2 flushed between steps (256 MB write)",
+                   "parallelism": f"{world} independent replica(s), sequences sharded by rank"},
+        "attn_tflops": attn_flops / attn_s / 1e12,
+        "attn_tbps": attn_bytes / attn_s / 1e12,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": (h_qn.numel() + h_qr.numel()) * 2 + h_idx.numel() * 4,
+                "d2h_bytes_per_step": h_out.numel() * 2,
+                "note": "pinned host q_nope/q_rope/index lists in, out back, every step; cache and weights resident"},
+        "gpu_launches": 3 * K,
+        "clocks": clocks.summary(),
+        "step_ms_min": min(step_ms),
+        "step_ms_median": statistics.median(step_ms),
+    }
+    print(json.dumps(line))
+
+
 # ------------------------------------------------------------------------- reference arm
 def main_reference(args):
     rank, world, local = dist_env()
@@ -595,9 +763,10 @@ def parse(argv=None):
     ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="decode", choices=["decode", "append"],
+    ap.add_argument("--op", default="decode", choices=["decode", "append", "sparse"],
                     help="decode: the absorbed decode step (headline); append: the cache append "
-                         "(latent down-projection of the new tokens, d_model = 7168)")
+                         "(latent down-projection of the new tokens, d_model = 7168); sparse: the decode "
+                         "step with sparse top-k attention (k = 2048, workload 'sparse' by default)")
     a = ap.parse_args(argv)
     if a.warmup < 3:
         a.warmup = 3

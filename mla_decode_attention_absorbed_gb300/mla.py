@@ -248,7 +248,7 @@ def cache_append(prob: Problem, x, w_dkv, k_rope, cache: Cache, workspace=None, 
     d = prob.dims()
     _check(lib.mla_cache_append(ctypes.byref(d), int(x.shape[-1]), _ptr(x), _ptr(w_dkv), _ptr(k_rope),
                                 ctypes.byref(cache), _ptr(workspace), workspace.numel(), _stream(stream)),
-           "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse")
+           "mla_cache_append")
     return workspace
 
 
