@@ -29,7 +29,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from mla_decode_attention_absorbed_gb300.workloads import CONFIGS, make_inputs  # noqa: E402
+from mla_decode_attention_absorbed_gb300.workloads import CONFIGS, KV_FP8_SCALE, make_inputs, to_fp8_cache  # noqa: E402
 
 METRIC = "MLA decode TFLOP/s, HBM TB/s & roofline fraction (H=128, d_c=512+64, 1×GB300)"
 DEFAULT_CONFIG = "dsv3"
@@ -76,12 +76,14 @@ def replica_seed(cfg_seed: int, rank: int) -> int:
 
 
 # ------------------------------------------------------------------------- algorithmic work
-def work(cfg, seq_lens):
+def work(cfg, seq_lens, kv_bytes: int = 2):
+    """Algorithmic FLOPs and bytes of one step; kv_bytes = bytes per cached element
+    (2 for bf16, 1 for an FP8 cache: the query, o_lat and lse stay as they are)."""
     from oracle import counts  # closed-form counters, pinned against the pages
     lens = [int(x) for x in seq_lens]
     B, H, s_q = cfg.B, cfg.H, cfg.s_q
     attn_f = counts.attention_flops(H, cfg.d_c, cfg.d_rope, lens, s_q)
-    attn_b = counts.attention_bytes(H, cfg.d_c, cfg.d_rope, lens, s_q)
+    attn_b = counts.attention_bytes(H, cfg.d_c, cfg.d_rope, lens, s_q) - sum(lens) * cfg.W * (2 - kv_bytes)
     abs_f = counts.absorb_flops(B, s_q, H, cfg.d_nope, cfg.d_c)
     abs_b = counts.absorb_bytes(B, s_q, H, cfg.d_nope, cfg.d_c, cfg.d_rope)
     out_f = counts.out_proj_flops(B, s_q, H, cfg.d_c, cfg.d_v)
@@ -89,7 +91,7 @@ def work(cfg, seq_lens):
     pairs = sum(counts.visible_pairs(L, s_q) for L in lens)
     return dict(attn_flops=attn_f, attn_bytes=attn_b, step_flops=attn_f + abs_f + out_f,
                 step_bytes=attn_b + abs_b + out_b, pairs=pairs, tokens=B * s_q,
-                cache_bytes=sum(lens) * (cfg.d_c + cfg.d_rope) * 2)
+                cache_bytes=sum(lens) * (cfg.d_c + cfg.d_rope) * kv_bytes)
 
 
 def peaks():
@@ -187,11 +189,15 @@ def run_ours(cfg, args, rank, world, local, active):
     mla.load()
     c = cfg.with_(seed=replica_seed(cfg.seed, rank))
     inp = make_inputs(c)
-    w = work(c, inp["seq_lens"].tolist())
+    kv_scale = None
+    if args.kv == "fp8":
+        inp["kv"] = to_fp8_cache(inp["kv"])
+        kv_scale = inp["kv_scale"] = KV_FP8_SCALE
+    w = work(c, inp["seq_lens"].tolist(), 1 if args.kv == "fp8" else 2)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     prob = mla.Problem.of(c)
     dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], c.page_size,
-                      max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits)
+                      max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=kv_scale)
     splits = mla.decode_num_splits(prob, dec.cache) if args.splits == 0 else args.splits
     q_nope, q_rope = d["q_nope"], d["q_rope"]
     stream = torch.cuda.current_stream(dev)
@@ -289,7 +295,7 @@ def cpu_baseline(cfg, inp, budget_s: float = 12.0):
             kv, bt = inp["kv"], inp["block_table"][b:b + 1]
         t0 = time.perf_counter()
         oracle.decode(sub, one["q_nope"], one["q_rope"], kv, one["seq_lens"], inp["w_uk"], inp["w_uv"],
-                      block_table=bt, page_size=cfg.page_size)
+                      block_table=bt, page_size=cfg.page_size, kv_scale=inp.get("kv_scale"))
         t_used += time.perf_counter() - t0
         L = int(one["seq_lens"][0])
         done_flops += (counts.attention_flops(cfg.H, cfg.d_c, cfg.d_rope, [L], cfg.s_q)
@@ -332,7 +338,8 @@ def main_ours(args):
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"]}
     roof["traffic"] = traffic_for(f"attn:{cfg.name}")
-    roof["kernel"] = "mla_decode_attn (split-T attention + LSE combine)"
+    roof["kernel"] = "mla_decode_attn (split-T attention + LSE combine)" + (
+        ", FP8 E4M3 cache dequantised on chip, fp16 MMAs" if args.kv == "fp8" else "")
     roof["peak_source"] = pk["source"] + (" burst bf16" if tensor_bound else " HBM copy")
     roof["roofline_time_us"] = max(w["attn_flops"] / (pk["bf16_tflops"] * 1e12),
                                    w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)) * 1e6
@@ -350,9 +357,10 @@ def main_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if args.kv == "bf16" else "e4m3 cache, f16 MMAs, bf16 projections",
         "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights)",
-        "config": {"workload": workload_name(cfg), "num_splits": r["splits"],
+        "config": {"workload": workload_name(cfg) + (", FP8 E4M3 cache (scale 1/16)" if args.kv == "fp8" else ""),
+                   "num_splits": r["splits"],
                    "l2": ("inputs larger than L2: the cache alone is "
                           f"{w['cache_bytes'] / 1e6:.0f} MB per replica") if w["cache_bytes"] >= 2 * L2_BYTES
                    else "L2 flushed between steps (256 MB write)",
@@ -545,7 +553,8 @@ def cpu_baseline_sparse(cfg, inp, idx, per_pair_flops, budget_s: float = 12.0):
         L = inp["seq_lens"][b:b + 1]
         t0 = time.perf_counter()
         q_cat = oracle.absorb_q(sub, inp["q_nope"][b:b + 1], inp["q_rope"][b:b + 1], inp["w_uk"])
-        o_lat, _ = oracle.attend_sparse(sub, q_cat, kv, L, idx[b:b + 1], bt, cfg.page_size)
+        o_lat, _ = oracle.attend_sparse(sub, q_cat, kv, L, idx[b:b + 1], bt, cfg.page_size,
+                                        kv_scale=inp.get("kv_scale"))
         oracle.out_proj(sub, o_lat, inp["w_uv"])
         t_used += time.perf_counter() - t0
         lim = int(L[0]) - cfg.s_q + torch.arange(cfg.s_q).view(-1, 1)
@@ -570,11 +579,16 @@ def main_sparse(args, cfg, rank, world, local, active):
     mla.load()
     c = cfg.with_(seed=replica_seed(cfg.seed, rank))
     inp = make_inputs(c)
+    kv_scale, eb = None, 2
+    if args.kv == "fp8":
+        inp["kv"] = to_fp8_cache(inp["kv"])
+        kv_scale, eb = KV_FP8_SCALE, 1
+        inp["kv_scale"] = kv_scale
     idx = make_sparse_indices(c, inp["seq_lens"], TOPK)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     d_idx = idx.to(dev)
     prob = mla.Problem.of(c)
-    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size)
+    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size, kv_scale=kv_scale)
     q_cat = torch.empty(c.B, c.s_q, c.H, c.W, dtype=torch.bfloat16, device=dev)
     o_lat = torch.empty(c.B, c.s_q, c.H, c.d_c, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(c.B, c.s_q, c.H, dtype=torch.float32, device=dev)
@@ -585,7 +599,7 @@ def main_sparse(args, cfg, rank, world, local, active):
                                         + torch.arange(c.s_q).view(1, -1, 1)))).sum())
     per_pair_flops = 2 * c.H * (c.W + c.d_c)
     attn_flops = n_pairs * per_pair_flops
-    attn_bytes = n_pairs * c.W * 2 + q_cat.numel() * 2 + o_lat.numel() * 2 + lse.numel() * 4 + idx.numel() * 4
+    attn_bytes = n_pairs * c.W * eb + q_cat.numel() * 2 + o_lat.numel() * 2 + lse.numel() * 4 + idx.numel() * 4
     proj_flops = 2 * c.B * c.s_q * c.H * c.d_nope * c.d_c + 2 * c.B * c.s_q * c.H * c.d_c * c.d_v
     step_flops = attn_flops + proj_flops
 
@@ -674,9 +688,11 @@ def main_sparse(args, cfg, rank, world, local, active):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if args.kv == "bf16" else "e4m3 cache, f16 MMAs, bf16 projections",
         "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights, uniform random top-k lists)",
-        "config": {"workload": f"{workload_name(c)}, top-{TOPK} lists", "num_splits": args.splits,
+        "config": {"workload": f"{workload_name(c)}, top-{TOPK} lists"
+                               + (", FP8 E4M3 cache (scale 1/16)" if args.kv == "fp8" else ""),
+                   "num_splits": args.splits,
                    "l2": "L2 flushed between steps (256 MB write)",
                    "parallelism": f"{world} independent replica(s), sequences sharded by rank"},
         "attn_tflops": attn_flops / attn_s / 1e12,
@@ -763,6 +779,8 @@ def parse(argv=None):
     ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="latent cache format of the decode and sparse ops (fp8: E4M3 codes, scale 1/16)")
     ap.add_argument("--op", default="decode", choices=["decode", "append", "sparse"],
                     help="decode: the absorbed decode step (headline); append: the cache append "
                          "(latent down-projection of the new tokens, d_model = 7168); sparse: the decode "

@@ -19,6 +19,8 @@
  *   mla_naive_decode the decompress-then-attend form, a comparison point only
  *                    ("The MLA decode speedup hiding in your model card",
  *                    section "The naive form, written out")
+ * The latent cache is bf16 or FP8 (E4M3 codes with one scale per cache), see
+ * mla_cache.
  *
  * Conventions for every entry point:
  *  - Pointers named for tensors are DEVICE pointers owned by the caller; the
@@ -82,17 +84,34 @@ typedef struct {
     float scale;  /* softmax scale */
 } mla_dims;
 
+/* Element formats of the latent cache (mla_cache.kv_dtype). */
+typedef enum {
+    MLA_KV_BF16 = 0,  /* bf16 values */
+    MLA_KV_E4M3 = 1   /* OCP FP8 E4M3 codes (1 sign, 4 exponent bits with bias 7,
+                         3 mantissa bits, no infinities, S.1111.111 = NaN); the
+                         value is kv_scale * code */
+} mla_kv_dtype;
+
 /* The latent cache: one row [c_kv (d_c) | k_rope (d_rope)] per cached token,
  * shared by every head ("Decode attention intensity is fixed at the
  * query-to-KV head ratio...", "A strong answer": 512 + 64 = 576 values, 1,152 B
- * in bf16).  seq_lens[b] counts the s_q new tokens, which are already
- * appended; query i (0-based) of sequence b sees tokens j <= seq_lens[b] - s_q + i. */
+ * in bf16, 576 B with an FP8 latent).  seq_lens[b] counts the s_q new tokens,
+ * which are already appended; query i (0-based) of sequence b sees tokens
+ * j <= seq_lens[b] - s_q + i.
+ * FP8 cache ("Decode attention intensity...", the FP8 row of the per-token
+ * table: one byte per element doubles the arithmetic intensity to 484 FLOP/B;
+ * the kernel dequantises on chip and computes in 16-bit): every element of
+ * every row, RoPE key included, is an E4M3 code, with one fp32 scale for the
+ * whole cache.  The attention kernels fold the scale into the query and the
+ * final normalisation, so |q_cat| * scale * log2(e) * kv_scale must stay below
+ * 65504 (the queries are carried in fp16).  d_c + d_rope must be a multiple of
+ * 16 and seq_stride a multiple of 16.  mla_naive_decode takes bf16 caches only. */
 typedef struct {
-    const void *kv;          /* bf16. block_table == NULL: contiguous, sequence b's
+    const void *kv;          /* kv_dtype elements. block_table == NULL: contiguous, sequence b's
                                 token j at kv + b*seq_stride + j*(d_c+d_rope).
                                 Otherwise the pool [num_pages][page_size][d_c+d_rope]. */
-    long long seq_stride;    /* contiguous: elements between sequences, a multiple of 8,
-                                >= capacity*(d_c+d_rope) */
+    long long seq_stride;    /* contiguous: elements between sequences, a multiple of 8
+                                (16 for FP8), >= capacity*(d_c+d_rope) */
     int capacity;            /* contiguous: tokens each sequence may hold */
     const int *block_table;  /* NULL => contiguous; else device int32 [B][max_pages]:
                                 token j of sequence b lives in pool page
@@ -103,6 +122,8 @@ typedef struct {
     const int *seq_lens;     /* device int32 [B] */
     int max_seq_len;         /* host upper bound of seq_lens used to plan the split;
                                 0 means capacity (contiguous) or max_pages*page_size */
+    int kv_dtype;            /* mla_kv_dtype; 0 (a zero-initialised descriptor) is bf16 */
+    float kv_scale;          /* MLA_KV_E4M3: value = kv_scale * code (finite, > 0); ignored for bf16 */
 } mla_cache;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -190,7 +211,8 @@ MLA_API size_t mla_cache_append_workspace_size(const mla_dims *dims, int d_model
  * w_dkv [d_model][d_c], k_rope [B][s_q][d_rope] (already rotated; the library
  * does no rotation).  The cache is described as for mla_decode_attn and its kv
  * buffer is WRITTEN (it must be writable device memory); only the new rows
- * change.  d_model must be a multiple of 8.  A length outside [s_q, capacity]
+ * change.  An FP8 cache receives the E4M3 code of value / kv_scale, rounded to
+ * nearest even and saturated to +-448, for every element of the row.  d_model must be a multiple of 8.  A length outside [s_q, capacity]
  * (MLA_ERR_SEQLEN) or a block-table entry outside the pool (MLA_ERR_PAGE) is
  * recorded in the workspace's status word and that token's row is not
  * written.  The weight is streamed once, split along d_model over the GPU. */

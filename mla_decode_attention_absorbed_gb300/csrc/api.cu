@@ -8,7 +8,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr int kMaxSplits = 64;
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (split planning only)
 constexpr size_t kStatusBytes = 256;  // status word + padding at the workspace start
@@ -41,6 +41,12 @@ int check_cache(const mla_dims *d, const mla_cache *c) {
     if (!c->kv || !c->seq_lens) return MLA_ERR_NULL;
     if (!aligned16(c->kv) || ((uintptr_t)c->seq_lens & 3u)) return MLA_ERR_ALIGN;
     const long long W = d->d_c + d->d_rope;
+    if (c->kv_dtype != MLA_KV_BF16 && c->kv_dtype != MLA_KV_E4M3) return MLA_ERR_UNSUPPORTED;
+    if (c->kv_dtype == MLA_KV_E4M3) {
+        // a positive, finite scale; rows and sequence strides of whole 16-byte units
+        if (!(c->kv_scale > 0.f) || c->kv_scale > 3.0e38f) return MLA_ERR_SHAPE;
+        if (W % 16 || (!c->block_table && c->seq_stride % 16)) return MLA_ERR_ALIGN;
+    }
     if (c->block_table) {
         if ((uintptr_t)c->block_table & 3u) return MLA_ERR_ALIGN;
         if (c->max_pages < 1 || c->page_size < 1 || c->num_pages < 1) return MLA_ERR_SHAPE;
@@ -105,7 +111,9 @@ mla::AttnParams make_params(const mla_dims *d, const mla_cache *c) {
     mla::AttnParams p;
     memset(&p, 0, sizeof p);
     p.B = d->B; p.H = d->H; p.s_q = d->s_q; p.d_c = d->d_c; p.d_rope = d->d_rope; p.scale = d->scale;
-    p.kv = (const __nv_bfloat16 *)c->kv;
+    p.kv = c->kv;
+    p.kv_fp8 = c->kv_dtype == MLA_KV_E4M3;
+    p.kv_scale = p.kv_fp8 ? c->kv_scale : 1.f;
     p.seq_stride = c->seq_stride;
     p.capacity = (int)cache_capacity(c);
     p.block_table = c->block_table;
@@ -209,6 +217,7 @@ MLA_API int mla_cache_append(const mla_dims *dims, int d_model, const void *x, c
     if (d_model % 8) return MLA_ERR_ALIGN;  // rows of x must be whole 16-byte units
     s = check_cache(dims, cache);
     if (s) return s;
+    if (cache->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     if (ws_bytes < mla_cache_append_workspace_size(dims, d_model)) return MLA_ERR_WORKSPACE;
@@ -294,6 +303,7 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
     if (s) return s;
     if (!cache) return MLA_ERR_NULL;
     if ((s = check_cache(dims, cache))) return s;
+    if (cache->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     if (ws_bytes < mla_naive_workspace_size(dims, cache)) return MLA_ERR_WORKSPACE;

@@ -25,12 +25,35 @@
 // a buffer is never refilled before it has been read, and no "buffer free"
 // signal has to cross the cluster.
 //
-// Tensor memory (512 columns): O [0, 256), S [256, 320), P (bf16) [320, 352),
-// Q slice (bf16, the A operand of the score MMA) [352, 512).
+// Three ways of feeding the tensor cores.
+//  - Dense bf16 cache: the producer's TMA tile loads write the 128-byte-swizzled
+//    operand tiles straight into a 4-stage ring.
+//  - Sparse lists over a bf16 cache: the listed rows are gathered straight into
+//    the same 4-stage ring by two engines at once -- the producer's
+//    tile::gather4 copies (four rows of one 128-byte box per copy) take the
+//    first two boxes of a row, and four loader warps take the rest with 16-byte
+//    cp.async copies (the tensor-memory-access unit alone moves one 4-row box in
+//    about 70 cycles, too slow for 80 boxes a tile).  Entries that take no part
+//    are gathered from row -1, which the copy engine fills with zeros.
+//  - FP8 caches: the producer copies each tile's row-major E4M3 codes into the
+//    top of the operand stage the tile will occupy -- one TMA copy per tile
+//    (dense), or one tile::gather4 copy per 4 listed rows (sparse), each moving
+//    this CTA's whole channel slice of a row as 32-bit elements -- and four
+//    converter warps rewrite the stage in place as swizzled fp16 tiles (the
+//    codes are exact in fp16), zeroing the rows that take no part.  The warps
+//    first load all their codes into registers and wait until every converter
+//    has, then store, so no code is overwritten before it is read; the 4-stage
+//    ring and the shared-memory footprint stay those of the bf16 kernel.  The
+//    MMAs run in fp16 (Q, P and the tile) and the cache's scale is folded into
+//    Q's pre-scale and into the final normalisation.
+//
+// Tensor memory (512 columns): O [0, 256), S [256, 320), P (16-bit) [320, 352),
+// Q slice (16-bit, the A operand of the score MMA) [352, 512).
 // Warps 0-7: softmax and epilogue, two warps per TMEM lane quadrant (warp w
 // owns rows 32*(w%4) .. +31 and token columns 32*(w/4) .. +31 of each tile);
 // warp 8: TMA producer; warp 9: TMEM owner, issues the score MMAs; warp 10:
-// ships the staged partial scores to the peer; warp 11: issues the sum MMAs.
+// ships the staged partial scores to the peer; warp 11: issues the sum MMAs;
+// warps 12-15: converters (FP8) or loaders (bf16 sparse).
 // Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT, drains what is in
 // flight, and the CTA returns.
 #include <cuda_fp16.h>
@@ -48,14 +71,45 @@ using namespace sm100;
 constexpr int kRows = 128;        // query rows per work item (MMA M)
 constexpr int kTile = 64;         // tokens per tile (MMA N of the score, K of the sum)
 constexpr int kHalf = kTile / 2;  // tokens per softmax thread
-constexpr int kStages = 4;        // tiles in flight
 constexpr int kMaxBoxes = 5;      // 64-channel boxes per tile and CTA (320 channels)
 constexpr int kBoxBytes = kTile * 128;
 constexpr int kStageBytes = kMaxBoxes * kBoxBytes;  // 40 KB
 constexpr int kXBytes = kRows * kTile * 2;          // one partial-score tile in fp16 (16 KB)
 constexpr int kSoftmaxThreads = 256;
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10, kSumWarp = 11;
-constexpr int kThreads = kSoftmaxThreads + 128;
+constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10, kSumWarp = 11, kConvWarp0 = 12;
+constexpr int kConvWarps = 4;     // loader warps (bf16 sparse)
+constexpr int kFp8ConvWarps = 4;  // converter warps (FP8)
+constexpr int kTmaBoxes = 2;      // bf16 sparse: boxes of a row gathered by tile::gather4
+
+constexpr int kRing = 4;          // operand-ring stages (tiles in flight into the MMAs)
+
+// threads of a variant
+__host__ __device__ constexpr int extra_warps(bool sparse, bool fp8) { return fp8 ? kFp8ConvWarps : (sparse ? kConvWarps : 0); }
+__host__ __device__ constexpr int threads_of(bool sparse, bool fp8) {
+    return kSoftmaxThreads + 128 + 32 * extra_warps(sparse, fp8);
+}
+
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory"); }
+
+// Register split of the 512-thread variants: the launch gives every thread
+// 65536 / 512 = 128 registers; the two softmax warpgroups raise theirs to 136
+// and the other two lower theirs to 120 (2 x 128 x 136 + 2 x 128 x 120 = 65536,
+// exactly the launch's total, so the raise never waits on registers nobody
+// gives up).  Each warpgroup runs its instruction once, on entering its roles.
+constexpr int kRegSoftmax = 136, kRegOther = 120;
+static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split must equal the launch's total");
+template <int kRegs>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs)); }
+template <int kRegs>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs)); }
+
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
 constexpr uint32_t kBarPairBase = 1;  // named barrier 1 + quadrant: the two warps of a quadrant (64 threads)
@@ -65,22 +119,25 @@ struct Geo {
     int kw;      // contraction width (multiple of 16)
     int nbox;    // 64-channel boxes loaded per tile
     int vn;      // latent columns this CTA accumulates (multiple of 64, <= 256)
+    int pitch;   // FP8: bytes of one raw row (the slice, rounded up to 32 B)
+    int x_u32;   // FP8: first 32-bit element of the slice within a cache row
 };
 
 struct Smem {
-    uint8_t kv[kStages][kStageBytes];
+    uint8_t kv[kRing][kStageBytes];  // swizzled operand tiles (FP8: raw codes first land at the top)
     // split mode: this CTA's scaled partial scores (fp16) staged for the bulk copy
     // to the peer, and the peer's received by tile parity.  Row r is 128 B (64
     // fp16); its 16-byte chunk c sits at chunk c ^ (r % 8).
-    __half tx[kRows * kTile];
+    alignas(128) __half tx[kRows * kTile];
     __half rx[2][kRows * kTile];
     // per half-row values the two warps of a quadrant exchange, by tile parity:
     // tile maxima in the loop, softmax sums in the epilogue
     float pair[2][2][kRows];
     int pair_stop[4][2];  // each quadrant's joint decision to leave the tile loop, by tile parity
-    // sparse: per stage, bit r set when row r of the tile is a listed, visible token
-    unsigned long long valid[kStages];
-    uint64_t full[kStages], empty[kStages];
+    // sparse and FP8: per stage, bit r set when row r of the tile takes part
+    unsigned long long valid[kRing];
+    uint64_t full[kRing], empty[kRing];
+    uint64_t landed[kRing], read[kRing];  // FP8: raw codes landed; every converter holds its codes
     uint64_t q_ready, s_full, s_free, p_ready, o_done, drain;
     uint64_t staged, tx_free, rx_full[2];
     uint32_t tmem_base;
@@ -96,8 +153,8 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Bounded wait that also gives up once the CTA is aborting.
-template <bool kCluster = false>
-__device__ __forceinline__ bool wait_bar(Smem &sm, uint64_t *bar, uint32_t parity) {
+template <bool kCluster = false, class S>
+__device__ __forceinline__ bool wait_bar(S &sm, uint64_t *bar, uint32_t parity) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     const long long c0 = clock64();
@@ -112,14 +169,14 @@ __device__ __forceinline__ bool wait_bar(Smem &sm, uint64_t *bar, uint32_t parit
 
 // Every lane waits; the warp proceeds only if all lanes saw the phase complete,
 // so warp-collective tcgen05 instructions that follow stay converged.
-template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait(Smem &sm, uint64_t *bar, uint32_t parity) {
+template <bool kCluster = false, class S>
+__device__ __forceinline__ bool warp_wait(S &sm, uint64_t *bar, uint32_t parity) {
     const bool ok = wait_bar<kCluster>(sm, bar, parity);
     return __all_sync(0xffffffffu, ok);
 }
 
-template <bool kSplit>
-__device__ __forceinline__ void raise_abort(Smem &sm, const AttnParams &p, uint32_t peer) {
+template <bool kSplit, class S>
+__device__ __forceinline__ void raise_abort(S &sm, const AttnParams &p, uint32_t peer) {
     *(volatile int *)&sm.abort = 1;
     set_status(p.status, MLA_ERR_TIMEOUT);
     if (kSplit) {
@@ -154,9 +211,75 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
     return __half22float2(h);
 }
 
-template <bool kSplit, bool kPaged, bool kSparse>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_tc(const __grid_constant__ CUtensorMap tm_kv, const AttnParams p, const Geo g0, const Geo g1) {
+// Four E4M3 codes (the bytes of u, lowest first) as four fp16 values (two
+// f16x2 words); every E4M3 value is an fp16 number, so this is exact.
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4(uint32_t u) {
+    uint2 r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\tcvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+        : "=r"(r.x), "=r"(r.y)
+        : "r"(u));
+    return r;
+}
+
+// Converter warp cw (of kNConv) turns its share of a raw FP8 tile (64 rows of
+// `pitch` bytes) into the fp16 operand stage.  Input chunk f of the tile (16
+// codes: row f / ncin, codes 16 (f % ncin) ..) becomes output chunks 2 (f % ncin)
+// and 2 (f % ncin) + 1 of that row (8 fp16 each); output chunk c of row r lands
+// at chunk (c % 8) ^ (r % 8) of row r of box c / 8.  The warp's input chunks are
+// all loaded first, so the loads overlap; `all_read()` then waits until every
+// converter holds its codes (the raw tile lies inside the stage being written)
+// and, if it returns false, nothing is stored.  Rows whose bit in vmask is
+// clear are written as zeros.
+template <int kNConv, class AllRead>
+__device__ __forceinline__ void convert_fp8_tile(uint8_t *dst, const uint8_t *src, int pitch, int ncin,
+                                                 unsigned long long vmask, int cw, int lane, AllRead &&all_read) {
+    constexpr int kMax = kTile * 20 / (32 * kNConv);  // input chunks per lane at 320 codes a row
+    const int per = kTile * ncin / kNConv;             // input chunks of this warp
+    // f / ncin through a float reciprocal: (f + 0.5) / ncin is at least 0.5 / 20
+    // away from an integer and the product errs by less than 1280 * 2^-23, so the
+    // truncation is the exact quotient (a division would cost a loop per chunk)
+    const float inv = 1.0f / (float)ncin;
+    auto row_of = [&](int i) { return (int)(((float)(cw * per + lane + 32 * i) + 0.5f) * inv); };
+    uint4 in[kMax];
+#pragma unroll
+    for (int i = 0; i < kMax; ++i) {
+        const int r = row_of(i), c = cw * per + lane + 32 * i - r * ncin;
+        in[i] = make_uint4(0, 0, 0, 0);
+        if (lane + 32 * i < per && ((vmask >> r) & 1ull)) in[i] = *reinterpret_cast<const uint4 *>(src + r * pitch + c * 16);
+    }
+    if (!all_read()) return;
+#pragma unroll
+    for (int i = 0; i < kMax; ++i) {
+        if (lane + 32 * i < per) {
+            const int r = row_of(i), c = cw * per + lane + 32 * i - r * ncin;
+            const uint2 a = e4m3x4_to_f16x4(in[i].x), b = e4m3x4_to_f16x4(in[i].y);
+            const uint2 d = e4m3x4_to_f16x4(in[i].z), e = e4m3x4_to_f16x4(in[i].w);
+            const int o0 = 2 * c, sw = r & 7;
+            uint8_t *row = dst + (o0 >> 3) * kBoxBytes + r * 128;
+            *reinterpret_cast<uint4 *>(row + (((o0 & 7) ^ sw) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+            *reinterpret_cast<uint4 *>(row + ((((o0 & 7) + 1) ^ sw) << 4)) = make_uint4(d.x, d.y, e.x, e.y);
+        }
+    }
+}
+
+// Instruction descriptor of the kernel's MMAs: bf16 operands, or fp16 for an FP8 cache.
+template <bool kFp8>
+__device__ __forceinline__ uint32_t idesc_of(int M, int N, bool a_mn, bool b_mn) {
+    const uint32_t d = idesc_bf16(M, N, a_mn, b_mn);
+    return kFp8 ? (d & ~((7u << 7) | (7u << 10))) : d;  // A / B format 0 = f16
+}
+
+template <bool kSplit, bool kPaged, bool kSparse, bool kFp8>
+__global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
+    attn_tc(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1, const AttnParams p,
+            const Geo g0, const Geo g1) {
+    constexpr bool kStaged = kFp8;                // converter warps
+    constexpr bool kLoaders = kSparse && !kFp8;   // loader warps share the gather
+    constexpr int kMma = kMmaWarp;
+    constexpr int kExch = kExchangeWarp;
+    constexpr int kNConv = kStaged ? kFp8ConvWarps : kConvWarps;
+    constexpr bool kRegSplit = threads_of(kSparse, kFp8) == 512;
     extern __shared__ uint8_t smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -164,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t rank = kSplit ? cluster_rank() : 0;
     const uint32_t peer = rank ^ 1u;
     const Geo g = rank == 0 ? g0 : g1;
+    const CUtensorMap *tm = rank == 0 ? &tm0 : &tm1;
     const int rb = kSplit ? blockIdx.x / 2 : blockIdx.x;
     const int split = blockIdx.y, b = blockIdx.z;
     const int rows_total = p.s_q * p.H;
@@ -176,9 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ntiles = (t1 - t0 + kTile - 1) / kTile;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
+        // the loaders of a CTA whose slice has no box past the gathered ones stay idle
+        const bool loading = kLoaders && g.nbox > kTmaBoxes;
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&sm.full[s], kStaged ? kNConv : (loading ? 1 + kConvWarps : 1));
             mbar_init(&sm.empty[s], 1);
+        }
+        if constexpr (kStaged) {
+            for (int s = 0; s < kRing; ++s) {
+                mbar_init(&sm.landed[s], 1);
+                mbar_init(&sm.read[s], kNConv);
+            }
         }
         mbar_init(&sm.q_ready, kSoftmaxThreads);
         mbar_init(&sm.s_full, 1);
@@ -194,231 +326,367 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.abort = 0;
         sm.armed = sm.received = -1;
         fence_mbar_init();
-        tma_prefetch_desc(&tm_kv);
+        tma_prefetch_desc(&tm0);
+        if (kSplit) tma_prefetch_desc(&tm1);
     }
     if (!seq_ok && split == 0 && rb == 0 && rank == 0 && threadIdx.x == 0) set_status(p.status, MLA_ERR_SEQLEN);
-    if (warp == kMmaWarp) tmem_alloc<512>(&sm.tmem_base);
+    if (warp == kMma) tmem_alloc<512>(&sm.tmem_base);
     tc_fence_before();
     if (kSplit) cluster_sync();
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == kProducerWarp && kSparse) {
-        // ------------------------------------------------------------ TMA producer, sparse
-        // Tile n = listed entries e = t0 + 64 n + r.  The whole warp resolves them
-        // (lanes r and r + 32): an entry takes part if it names a token this row
-        // block's query may see, 0 <= j <= L - s_q + i (all rows of a block share
-        // i), on a page inside the pool; its cache row is gathered by tile::gather4
-        // (4 rows per copy, lanes 0-15).  Rows of entries that take no part are
-        // read from row 0 and zeroed by the score issuer before the MMAs.
-        const int W = p.d_c + p.d_rope;
-        const int iq = (rb * kRows) / p.H;
-        const int lim = L - p.s_q + iq;
-        const int *list = p.indices + ((long long)b * p.s_q + iq) * p.topk;
-        const long long seq_rows = p.seq_stride / W;  // contiguous: rows between sequences
-        int issued = 0;
-        for (int n = 0; n < ntiles; ++n) {
-            const int s = n % kStages;
-            if (n >= kStages && !warp_wait(sm, &sm.empty[s], ((n / kStages) - 1) & 1)) {
-                if (lane == 0) raise_abort<kSplit>(sm, p, peer);
-                break;
-            }
-            int rows[2];
-            bool vis[2];
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int e = t0 + n * kTile + lane + 32 * h2;
-                const int j = e < t1 ? __ldg(list + e) : -1;
-                vis[h2] = j >= 0 && j <= lim;
-                long long row = 0;
-                if (vis[h2]) {
-                    if (kPaged) {
-                        const int page = __ldg(p.block_table + (long long)b * p.max_pages + j / p.page_size);
-                        if (page >= 0 && page < p.num_pages) {
-                            row = (long long)page * p.page_size + j % p.page_size;
-                        } else {
-                            set_status(p.status, MLA_ERR_PAGE);
-                            vis[h2] = false;
-                        }
-                    } else {
-                        row = b * seq_rows + j;
-                    }
+    if (warp >= kSoftmaxWarps) {
+        if constexpr (kRegSplit) regs_dec<kRegOther>();
+        if (warp == kProducerWarp && kSparse) {
+            // ------------------------------------------------------------ producer, sparse
+            // Tile n = listed entries e = t0 + 64 n + r.  The whole warp resolves them
+            // (lanes r and r + 32): an entry takes part if it names a token this row
+            // block's query may see, 0 <= j <= L - s_q + i (all rows of a block share
+            // i), on a page inside the pool.  Lanes 0-15 then gather rows 4q .. 4q+3
+            // with tile::gather4: FP8, the whole slice of each row into the raw ring;
+            // bf16, the first kTmaBoxes 128-byte boxes of each row into the operand
+            // stage (the loader warps copy the rest).  Entries that take no part are
+            // gathered from row -1, which reads as zeros.  The next tile's entries are
+            // loaded one tile ahead, so their latency hides behind the wait for a
+            // free stage.
+            const int W = p.d_c + p.d_rope;
+            const int iq = (rb * kRows) / p.H;
+            const int lim = L - p.s_q + iq;
+            const int *list = p.indices + ((long long)b * p.s_q + iq) * p.topk;
+            const long long seq_rows = p.seq_stride / W;  // contiguous: rows between sequences
+            const int nbt = min(g.nbox, kTmaBoxes);
+            auto fetch = [&](int n, int (&j)[2]) {
+    #pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int e = t0 + n * kTile + lane + 32 * h2;
+                    j[h2] = (n < ntiles && e < t1) ? __ldg(list + e) : -1;
                 }
-                rows[h2] = vis[h2] ? (int)row : 0;
-            }
-            const unsigned lo = __ballot_sync(0xffffffffu, vis[0]), hi = __ballot_sync(0xffffffffu, vis[1]);
-            if (lane == 0) {
-                sm.valid[s] = (unsigned long long)hi << 32 | lo;
-                mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
-            }
-            __syncwarp();
-            // lane q (< 16) gathers rows 4q .. 4q + 3 of every box
-            int r4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int r = 4 * (lane & 15) + k;
-                const int a0 = __shfl_sync(0xffffffffu, rows[0], r & 31);
-                const int a1 = __shfl_sync(0xffffffffu, rows[1], r & 31);
-                r4[k] = r < 32 ? a0 : a1;
-            }
-            if (lane < 16)
-                for (int bx = 0; bx < g.nbox; ++bx)
-                    tma_gather4(sm.kv[s] + bx * kBoxBytes + lane * 4 * 128, &tm_kv, &sm.full[s], g.k0 + 64 * bx, r4[0],
-                                r4[1], r4[2], r4[3]);
-            issued = n + 1;
-        }
-        // every issued copy must land before this CTA may exit
-        const int first = issued > kStages ? issued - kStages : 0;
-        for (int n = first; n < issued; ++n) mbar_wait(&sm.full[n % kStages], (n / kStages) & 1);
-    } else if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            // y / z coordinates of tile n's box, or false if its page is outside the pool
-            auto coords = [&](int n, int &y, int &z) -> bool {
-                const int tok = t0 + n * kTile;
-                if (kPaged) {
-                    const int page = __ldg(p.block_table + (long long)b * p.max_pages + tok / p.page_size);
-                    y = page * p.page_size + tok % p.page_size;
-                    z = 0;
-                    return page >= 0 && page < p.num_pages;
-                }
-                y = tok;
-                z = b;
-                return true;
             };
+            int nxt[2];
+            fetch(0, nxt);
             int issued = 0;
             for (int n = 0; n < ntiles; ++n) {
-                const int s = n % kStages;
-                if (n >= kStages && !wait_bar(sm, &sm.empty[s], ((n / kStages) - 1) & 1)) {
-                    raise_abort<kSplit>(sm, p, peer);
+                const int s = n % kRing;
+                const int cur[2] = {nxt[0], nxt[1]};
+                fetch(n + 1, nxt);
+                if (n >= kRing && !warp_wait(sm, &sm.empty[s], ((n / kRing) - 1) & 1)) {
+                    if (lane == 0) raise_abort<kSplit>(sm, p, peer);
                     break;
                 }
-                int y, z;
-                if (!coords(n, y, z)) {
-                    set_status(p.status, MLA_ERR_PAGE);
-                    y = p.num_pages * p.page_size;  // wholly out of range: the box reads as zeros
+                int rows[2];
+                bool vis[2];
+    #pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int j = cur[h2];
+                    vis[h2] = j >= 0 && j <= lim;
+                    long long row = -1;
+                    if (vis[h2]) {
+                        if (kPaged) {
+                            const int page = __ldg(p.block_table + (long long)b * p.max_pages + j / p.page_size);
+                            if (page >= 0 && page < p.num_pages) {
+                                row = (long long)page * p.page_size + j % p.page_size;
+                            } else {
+                                set_status(p.status, MLA_ERR_PAGE);
+                                vis[h2] = false;
+                            }
+                        } else {
+                            row = b * seq_rows + j;
+                        }
+                    }
+                    rows[h2] = vis[h2] ? (int)row : -1;
                 }
-                mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
-                for (int bx = 0; bx < g.nbox; ++bx) {
-                    if (kPaged) tma_load_2d(sm.kv[s] + bx * kBoxBytes, &tm_kv, &sm.full[s], g.k0 + 64 * bx, y);
-                    else tma_load_3d(sm.kv[s] + bx * kBoxBytes, &tm_kv, &sm.full[s], g.k0 + 64 * bx, y, z);
+                const unsigned lo = __ballot_sync(0xffffffffu, vis[0]), hi = __ballot_sync(0xffffffffu, vis[1]);
+                const unsigned long long vmask = (unsigned long long)hi << 32 | lo;
+                if (lane == 0) {
+                    sm.valid[s] = vmask;
+                    if (kStaged) mbar_arrive_expect_tx(&sm.landed[s], kTile * g.pitch);
+                    else mbar_arrive_expect_tx(&sm.full[s], nbt * kBoxBytes);
+                }
+                __syncwarp();
+                // lane q (< 16) gathers rows 4q .. 4q + 3
+                int r4[4];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * (lane & 15) + k;
+                    const int a0 = __shfl_sync(0xffffffffu, rows[0], r & 31);
+                    const int a1 = __shfl_sync(0xffffffffu, rows[1], r & 31);
+                    r4[k] = r < 32 ? a0 : a1;
+                }
+                if (lane < 16) {
+                    if (kStaged) {
+                        tma_gather4(sm.kv[s] + kStageBytes - kTile * g.pitch + lane * 4 * g.pitch, tm, &sm.landed[s], g.x_u32, r4[0],
+                                    r4[1], r4[2], r4[3]);
+                    } else {
+                        for (int bx = 0; bx < nbt; ++bx)
+                            tma_gather4(sm.kv[s] + bx * kBoxBytes + lane * 4 * 128, tm, &sm.full[s], g.k0 + 64 * bx, r4[0],
+                                        r4[1], r4[2], r4[3]);
+                    }
                 }
                 issued = n + 1;
             }
             // every issued copy must land before this CTA may exit
-            const int first = issued > kStages ? issued - kStages : 0;
-            for (int n = first; n < issued; ++n) mbar_wait(&sm.full[n % kStages], (n / kStages) & 1);
-        }
-    } else if (warp == kMmaWarp || warp == kSumWarp) {
-        // ------------------------------------------------------------ MMA issuers
-        // Two independent streams share the tensor pipe: the scores (warp 9: tile
-        // k needs tile k loaded and S(k-1) read by the softmax) and the sums (warp
-        // 11: tile k needs P(k)).  Each score MMA accumulates into the previous
-        // one's result and waits out its latency; with the sums issued from a
-        // warp of their own they run in those gaps instead of queueing behind the
-        // whole chain (an issuing thread's next shared-memory operation waits for
-        // its queued MMAs, so one thread cannot keep both streams in flight).
-        const bool scores = warp == kMmaWarp;
-        const uint32_t idesc_qk = idesc_bf16(kRows, kTile, false, false);
-        const uint32_t idesc_pv = idesc_bf16(kRows, g.vn, false, true);
-        // descriptors of stage 0; a stage's are 16-byte-unit offsets of these
-        const uint64_t qk_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
-        const uint64_t pv_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), kBoxBytes, 1024);
-        const int nks = g.kw / 16;
-        bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
-        for (int n = 0; ok && n < ntiles; ++n) {
-            const int s = n % kStages;
-            if (scores) {
-                if (!warp_wait(sm, &sm.full[s], (n / kStages) & 1) || (n > 0 && !warp_wait(sm, &sm.s_free, (n - 1) & 1))) {
-                    ok = false;
-                    break;
+            const int first = issued > kRing ? issued - kRing : 0;
+            for (int n = first; n < issued; ++n)
+                mbar_wait(kStaged ? &sm.landed[n % kRing] : &sm.full[n % kRing], (n / kRing) & 1);
+        } else if (warp == kProducerWarp) {
+            // ------------------------------------------------------------ TMA producer, dense
+            if (lane == 0) {
+                // y / z coordinates of tile n's box, or false if its page is outside the pool
+                auto coords = [&](int n, int &y, int &z) -> bool {
+                    const int tok = t0 + n * kTile;
+                    if (kPaged) {
+                        const int page = __ldg(p.block_table + (long long)b * p.max_pages + tok / p.page_size);
+                        y = page * p.page_size + tok % p.page_size;
+                        z = 0;
+                        return page >= 0 && page < p.num_pages;
+                    }
+                    y = tok;
+                    z = b;
+                    return true;
+                };
+                int issued = 0;
+                for (int n = 0; n < ntiles; ++n) {
+                    const int s = n % kRing;
+                    if (n >= kRing && !wait_bar(sm, &sm.empty[s], ((n / kRing) - 1) & 1)) {
+                        raise_abort<kSplit>(sm, p, peer);
+                        break;
+                    }
+                    int y, z;
+                    const bool page_ok = coords(n, y, z);
+                    if (!page_ok) {
+                        set_status(p.status, MLA_ERR_PAGE);
+                        y = p.num_pages * p.page_size;  // wholly out of range: the box reads as zeros
+                    }
+                    if constexpr (kStaged) {
+                        // one box of 64 rows of this CTA's slice; rows past the sequence end
+                        // (which may hold anything) and a bad page's rows are zeroed by the converters
+                        const int cnt = page_ok ? min(kTile, L - (t0 + n * kTile)) : 0;
+                        sm.valid[s] = cnt >= kTile ? ~0ull : ((1ull << cnt) - 1ull);
+                        mbar_arrive_expect_tx(&sm.landed[s], kTile * g.pitch);
+                        uint8_t *raw = sm.kv[s] + kStageBytes - kTile * g.pitch;
+                        if (kPaged) tma_load_2d(raw, tm, &sm.landed[s], g.x_u32, y);
+                        else tma_load_3d(raw, tm, &sm.landed[s], g.x_u32, y, z);
+                    } else {
+                        mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
+                        for (int bx = 0; bx < g.nbox; ++bx) {
+                            if (kPaged) tma_load_2d(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y);
+                            else tma_load_3d(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y, z);
+                        }
+                    }
+                    issued = n + 1;
                 }
-                // tokens at or past the sequence end may hold anything (even NaN):
-                // zero them so that 0-weight products stay 0
-                if (kSparse) {
-                    // rows of entries that take no part were read from row 0: zero them
-                    const unsigned long long dead = ~sm.valid[s];
-                    if (dead) {
-                        for (int e = lane; e < kTile * 8 * g.nbox; e += 32) {
-                            const int rr = (e / 8) % kTile;
-                            if ((dead >> rr) & 1ull)
-                                reinterpret_cast<uint4 *>(sm.kv[s] + (e / (8 * kTile)) * kBoxBytes + rr * 128)[e % 8] =
-                                    make_uint4(0, 0, 0, 0);
+                // every issued copy must land before this CTA may exit
+                const int first = issued > kRing ? issued - kRing : 0;
+                for (int n = first; n < issued; ++n)
+                    mbar_wait(kStaged ? &sm.landed[n % kRing] : &sm.full[n % kRing], (n / kRing) & 1);
+            }
+        } else if (warp == kMma || warp == kSumWarp) {
+            // ------------------------------------------------------------ MMA issuers
+            // Two independent streams share the tensor pipe: the scores (warp 9: tile
+            // k needs tile k loaded and S(k-1) read by the softmax) and the sums (warp
+            // 11: tile k needs P(k)).  Each score MMA accumulates into the previous
+            // one's result and waits out its latency; with the sums issued from a
+            // warp of their own they run in those gaps instead of queueing behind the
+            // whole chain (an issuing thread's next shared-memory operation waits for
+            // its queued MMAs, so one thread cannot keep both streams in flight).
+            const bool scores = warp == kMma;
+            const uint32_t idesc_qk = idesc_of<kFp8>(kRows, kTile, false, false);
+            const uint32_t idesc_pv = idesc_of<kFp8>(kRows, g.vn, false, true);
+            // descriptors of stage 0; a stage's are 16-byte-unit offsets of these
+            const uint64_t qk_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
+            const uint64_t pv_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), kBoxBytes, 1024);
+            const int nks = g.kw / 16;
+            bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
+            for (int n = 0; ok && n < ntiles; ++n) {
+                const int s = n % kRing;
+                if (scores) {
+                    if (!warp_wait(sm, &sm.full[s], (n / kRing) & 1) || (n > 0 && !warp_wait(sm, &sm.s_free, (n - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    // tokens at or past the sequence end may hold anything (even NaN):
+                    // zero them so that 0-weight products stay 0 (the converters, and
+                    // the sparse gathers, already wrote zeros there)
+                    const int tok = t0 + n * kTile;
+                    const int valid = min(kTile, L - tok);
+                    if (!kStaged && !kSparse && valid < kTile) {
+                        for (int e = lane; e < (kTile - valid) * 8 * g.nbox; e += 32) {
+                            const int bx = e / ((kTile - valid) * 8);
+                            const int rr = valid + (e / 8) % (kTile - valid);
+                            reinterpret_cast<uint4 *>(sm.kv[s] + bx * kBoxBytes + rr * 128)[e % 8] = make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
                     }
-                }
-                const int tok = t0 + n * kTile;
-                const int valid = kSparse ? kTile : min(kTile, L - tok);
-                if (valid < kTile) {
-                    for (int e = lane; e < (kTile - valid) * 8 * g.nbox; e += 32) {
-                        const int bx = e / ((kTile - valid) * 8);
-                        const int rr = valid + (e / 8) % (kTile - valid);
-                        reinterpret_cast<uint4 *>(sm.kv[s] + bx * kBoxBytes + rr * 128)[e % 8] = make_uint4(0, 0, 0, 0);
+                    tc_fence_after();
+                    if (lane == 0) {
+                        // fully unrolled: each MMA is an immediate add to the descriptor and
+                        // the A address
+                        const uint64_t db = qk_desc0 + (uint64_t)((s * kStageBytes) >> 4);
+                        const uint32_t d_s = tmem + kColS, a_q = tmem + kColQ;
+    #pragma unroll
+                        for (int ks = 0; ks < kMaxBoxes * 4; ++ks)
+                            if (ks < nks)
+                                mma_ts(d_s, a_q + ks * 8, db + (uint64_t)(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4),
+                                       idesc_qk, ks > 0);
+                        mma_commit(&sm.s_full);
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                } else {
+                    if (!warp_wait(sm, &sm.p_ready, n & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {  // O += P(n) . V(n), then release the tile's stage
+                        const uint64_t db = pv_desc0 + (uint64_t)((s * kStageBytes) >> 4);
+    #pragma unroll
+                        for (int kt = 0; kt < kTile / 16; ++kt)
+                            mma_ts(tmem + kColO, tmem + kColP + kt * 8, db + (uint64_t)(kt * (16 * 128 / 16)), idesc_pv,
+                                   (n > 0) || kt > 0);
+                        mma_commit(&sm.o_done);
+                        mma_commit(&sm.empty[s]);
+                    }
                 }
-                tc_fence_after();
-                if (lane == 0) {
-                    // fully unrolled: each MMA is an immediate add to the descriptor and
-                    // the A address
-                    const uint64_t db = qk_desc0 + (uint64_t)((s * kStageBytes) >> 4);
-                    const uint32_t d_s = tmem + kColS, a_q = tmem + kColQ;
-#pragma unroll
-                    for (int ks = 0; ks < kMaxBoxes * 4; ++ks)
-                        if (ks < nks)
-                            mma_ts(d_s, a_q + ks * 8, db + (uint64_t)(((ks >> 2) * kBoxBytes + (ks & 3) * 32) >> 4),
-                                   idesc_qk, ks > 0);
-                    mma_commit(&sm.s_full);
-                }
-            } else {
-                if (!warp_wait(sm, &sm.p_ready, n & 1)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) {  // O += P(n) . V(n), then release the tile's stage
-                    const uint64_t db = pv_desc0 + (uint64_t)((s * kStageBytes) >> 4);
-#pragma unroll
-                    for (int kt = 0; kt < kTile / 16; ++kt)
-                        mma_ts(tmem + kColO, tmem + kColP + kt * 8, db + (uint64_t)(kt * (16 * 128 / 16)), idesc_pv,
-                               (n > 0) || kt > 0);
-                    mma_commit(&sm.o_done);
-                    mma_commit(&sm.empty[s]);
+                __syncwarp();
+            }
+            if (!ok) raise_abort<kSplit>(sm, p, peer);
+            // every MMA issued above must finish before tensor memory is released
+            if (lane == 0) mma_commit(&sm.drain);
+            __syncwarp();
+            mbar_wait(&sm.drain, 0);  // time-bounded only: in-flight MMAs must land
+            __syncwarp();
+        } else if (warp == kExch) {
+            // ------------------------------------------------------------ score exchange (split mode)
+            // Ships each staged tile of partial scores to the peer with one bulk copy
+            // that completes on the peer's receive barrier, then frees the staging buffer.
+            if (kSplit && lane == 0) {
+                const uint32_t rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
+                const uint32_t rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
+                for (int u = 0; u < ntiles; ++u) {
+                    if (!wait_bar(sm, &sm.staged, u & 1)) {
+                        raise_abort<kSplit>(sm, p, peer);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&sm.rx_full[u & 1], kXBytes);  // arm this CTA's receive of tile u
+                    *(volatile int *)&sm.armed = u;
+                    bulk_copy_to_peer(rx_peer0 + (u & 1) * (uint32_t)sizeof(sm.rx[0]), sm.tx, kXBytes,
+                                      rxfull_peer0 + (u & 1) * (uint32_t)sizeof(uint64_t));
+                    bulk_commit();
+                    bulk_wait_read_all();
+                    mbar_arrive(&sm.tx_free);
                 }
             }
-            __syncwarp();
-        }
-        if (!ok) raise_abort<kSplit>(sm, p, peer);
-        // every MMA issued above must finish before tensor memory is released
-        if (lane == 0) mma_commit(&sm.drain);
-        __syncwarp();
-        mbar_wait(&sm.drain, 0);  // time-bounded only: in-flight MMAs must land
-        __syncwarp();
-    } else if (warp == kExchangeWarp) {
-        // ------------------------------------------------------------ score exchange (split mode)
-        // Ships each staged tile of partial scores to the peer with one bulk copy
-        // that completes on the peer's receive barrier, then frees the staging buffer.
-        if (kSplit && lane == 0) {
-            const uint32_t rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
-            const uint32_t rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
-            for (int u = 0; u < ntiles; ++u) {
-                if (!wait_bar(sm, &sm.staged, u & 1)) {
-                    raise_abort<kSplit>(sm, p, peer);
+        } else if (warp >= kConvWarp0 && kLoaders) {
+            // ------------------------------------------------------------ loaders (bf16 sparse)
+            // Boxes kTmaBoxes .. nbox-1 of every listed row, copied 16 bytes at a time
+            // with cp.async straight into the swizzled stage (chunk c of row r goes to
+            // chunk (c % 8) ^ (r % 8) of row r of box c / 8).  Loader warp lw owns rows
+            // 16 lw .. 16 lw + 15 and resolves their entries itself (lanes 0-15, one
+            // tile ahead), the lanes running along a row's chunks; rows of entries that
+            // take no part are written as zeros.  Each iteration first announces tile
+            // n - 2, once its copies have landed (wait_group 1) and a proxy fence has
+            // made them visible to the tensor cores, and only then waits for a free
+            // stage, so two tiles of copies stay in flight.
+            const int lw = warp - kConvWarp0;
+            const int W = p.d_c + p.d_rope;
+            const int iq = (rb * kRows) / p.H;
+            const int lim = L - p.s_q + iq;
+            const int *list = p.indices + ((long long)b * p.s_q + iq) * p.topk;
+            const long long seq_rows = p.seq_stride / W;
+            const int c0 = 8 * kTmaBoxes;  // first chunk of a row the loaders copy
+            const int nl = g.kw / 8 - c0;  // chunks per row they copy (even)
+            const __nv_bfloat16 *kvb = static_cast<const __nv_bfloat16 *>(p.kv);
+            auto entry = [&](int n) -> int {  // lanes 0-15: list entry of row 16 lw + lane of tile n
+                const int e = t0 + n * kTile + 16 * lw + (lane & 15);
+                return (n < ntiles && e < t1) ? __ldg(list + e) : -1;
+            };
+            if (nl > 0) {
+                int nxt = entry(0);
+                for (int n = 0; n < ntiles + 2; ++n) {
+                    if (n >= 2) {  // announce tile n - 2 (n groups committed so far)
+                        cp_async_wait<1>();
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sm.full[(n - 2) % kRing]);
+                    }
+                    bool stop = false;
+                    if (n < ntiles) {
+                        const int j = nxt;
+                        nxt = entry(n + 1);
+                        long long myrow = -1;  // row of this lane's entry, -1: takes no part
+                        if (j >= 0 && j <= lim) {
+                            if (kPaged) {
+                                const int page = __ldg(p.block_table + (long long)b * p.max_pages + j / p.page_size);
+                                if (page >= 0 && page < p.num_pages) myrow = (long long)page * p.page_size + j % p.page_size;
+                            } else {
+                                myrow = b * seq_rows + j;
+                            }
+                        }
+                        const int s = n % kRing;
+                        if (n >= kRing && !warp_wait(sm, &sm.empty[s], ((n / kRing) - 1) & 1)) {
+                            if (lane == 0) raise_abort<kSplit>(sm, p, peer);
+                            stop = true;
+                        } else {
+                            const uint32_t stage = smem_u32(sm.kv[s]);
+                            int r = lane / nl, c = lane % nl;  // element lane of 16 rows x nl chunks
+                            for (int it = 0; it < 16 * nl / 32; ++it) {
+                                const long long grow = __shfl_sync(0xffffffffu, myrow, r);
+                                const int rr = 16 * lw + r, cc = c0 + c;
+                                const uint32_t dst = stage + (cc >> 3) * kBoxBytes + rr * 128 + (((cc & 7) ^ (rr & 7)) << 4);
+                                if (grow >= 0) {
+                                    cp_async16(dst, kvb + grow * W + g.k0 + cc * 8);
+                                } else {
+                                    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0) : "memory");
+                                }
+                                c += 32;
+                                while (c >= nl) {
+                                    c -= nl;
+                                    ++r;
+                                }
+                            }
+                        }
+                    }
+                    cp_async_commit();
+                    if (__any_sync(0xffffffffu, stop)) break;
+                }
+                cp_async_wait<0>();  // no copy may land after this CTA exits
+            }
+        } else if (warp >= kConvWarp0 && kStaged) {
+            // ------------------------------------------------------------ converters (FP8)
+            // Tile n's codes land at the top of stage n % 4 (the producer copied them
+            // there once the stage was free); the converters load them, agree that
+            // all have (mbarrier read[s]), rewrite the stage as fp16 operand tiles
+            // and announce it.
+            const int cw = warp - kConvWarp0;
+            const int ncin = g.kw / 16;  // 16-byte input chunks (16 codes) of a row
+            for (int n = 0; n < ntiles; ++n) {
+                const int s = n % kRing;
+                const uint32_t par = (n / kRing) & 1;
+                if (!warp_wait(sm, &sm.landed[s], par)) {
+                    if (lane == 0) raise_abort<kSplit>(sm, p, peer);
                     break;
                 }
-                mbar_arrive_expect_tx(&sm.rx_full[u & 1], kXBytes);  // arm this CTA's receive of tile u
-                *(volatile int *)&sm.armed = u;
-                bulk_copy_to_peer(rx_peer0 + (u & 1) * (uint32_t)sizeof(sm.rx[0]), sm.tx, kXBytes,
-                                  rxfull_peer0 + (u & 1) * (uint32_t)sizeof(uint64_t));
-                bulk_commit();
-                bulk_wait_read_all();
-                mbar_arrive(&sm.tx_free);
+                bool ok = true;
+                convert_fp8_tile<kNConv>(sm.kv[s], sm.kv[s] + kStageBytes - kTile * g.pitch, g.pitch, ncin,
+                                         sm.valid[s], cw, lane, [&]() {
+                                             __syncwarp();
+                                             if (lane == 0) mbar_arrive(&sm.read[s]);  // release: the loads are done
+                                             ok = warp_wait(sm, &sm.read[s], par);
+                                             return ok;
+                                         });
+                if (!ok) {
+                    if (lane == 0) raise_abort<kSplit>(sm, p, peer);
+                    break;
+                }
+                fence_proxy_async_smem();  // the MMAs read the stage through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.full[s]);
             }
         }
     } else {
+        if constexpr (kRegSplit) regs_inc<kRegSoftmax>();
         // ------------------------------------------------------------ softmax + epilogue
         const int quad = warp & 3, hf = warp >> 2;
         const int r = quad * 32 + lane;  // this thread's row == TMEM lane
@@ -427,13 +695,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qi = row_ok ? gr / p.H : 0;
         const int lim = L - p.s_q + qi;  // last visible token of this row
         const uint32_t lane_base = tmem_lane_base(quad);
-        const float scale_log2 = p.scale * 1.4426950408889634f;
+        // an FP8 cache's scale multiplies every key element: fold it into Q
+        const float scale_log2 = p.scale * 1.4426950408889634f * (kFp8 ? p.kv_scale : 1.f);
         const int W = p.d_c + p.d_rope;
         const uint32_t pair_bar = kBarPairBase + quad;
 
-        // Q slice -> TMEM (bf16 pairs), pre-multiplied by scale * log2(e) so that the
-        // score MMAs produce exponents in log2 units directly; the two warps of a
-        // quadrant take alternate 32-channel chunks; padding rows and channels are zero
+        // Q slice -> TMEM (bf16 pairs, fp16 with an FP8 cache), pre-multiplied by
+        // scale * log2(e) (* kv_scale) so that the score MMAs produce exponents in
+        // log2 units directly; the two warps of a quadrant take alternate
+        // 32-channel chunks; padding rows and channels are zero
         {
             const __nv_bfloat16 *qrow = p.q_cat + ((long long)b * rows_total + gr) * W;
             for (int c0 = 32 * hf; c0 < g.kw; c0 += 64) {
@@ -448,7 +718,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < 4; ++k) {
                         const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[k]);
                         const float2 f = __bfloat1622float2(h);
-                        v[e * 4 + k] = pack_bf16x2(f.x * scale_log2, f.y * scale_log2);
+                        v[e * 4 + k] = kFp8 ? pack_f16x2(f.x * scale_log2, f.y * scale_log2)
+                                            : pack_bf16x2(f.x * scale_log2, f.y * scale_log2);
                     }
                 }
                 tmem_st16(tmem + lane_base + kColQ + c0 / 2, v);
@@ -540,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_ok = page >= 0 && page < p.num_pages;  // tokens of a bad page are skipped
             }
             // sparse: the producer's per-row flags (listed, visible to this block's query, good page)
-            const unsigned long long vmask = kSparse ? sm.valid[n % kStages] : 0ull;
+            const unsigned long long vmask = kSparse ? sm.valid[n % kRing] : 0ull;
             const bool whole = kSparse ? vmask == ~0ull
                                        : tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q;
             float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -591,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float c = ex2(x[j + 1] - m_use);
                     sum0 += a;
                     sum1 += c;
-                    pk[j / 2] = pack_bf16x2(a, c);
+                    pk[j / 2] = kFp8 ? pack_f16x2(a, c) : pack_bf16x2(a, c);
                 }
             }
             l = l * alpha + (sum0 + sum1);
@@ -643,8 +914,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float ln2 = 0.6931471805599453f;
         const int half_cols = g.vn / 2;
         const bool any = have_o && l_row > 0.f;
+        // an FP8 cache's scale multiplies every value element
+        const float vscale = kFp8 ? p.kv_scale : 1.f;
         if (p.num_splits == 1) {
-            const float inv = any ? 1.f / l_row : 0.f;
+            const float inv = any ? vscale / l_row : 0.f;
             __nv_bfloat16 *dst = p.o_lat + ((long long)b * rows_total + gr) * p.d_c + g.k0;
             for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
@@ -674,8 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4 *d4 = reinterpret_cast<float4 *>(dst + c);
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        d4[e] = any ? make_float4(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
-                                                  __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]))
+                        d4[e] = any ? make_float4(__uint_as_float(u[4 * e]) * vscale, __uint_as_float(u[4 * e + 1]) * vscale,
+                                                  __uint_as_float(u[4 * e + 2]) * vscale,
+                                                  __uint_as_float(u[4 * e + 3]) * vscale)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
@@ -694,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(&sm.rx_full[u & 1], (u >> 1) & 1);
     }
     if (kSplit) cluster_sync();  // the peer may still touch this CTA's shared memory until here
-    if (warp == kMmaWarp) {
+    if (warp == kMma) {
         tc_fence_after();
         tmem_free<512>(tmem);
     }
@@ -702,6 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 Geo make_geo(const AttnParams &p, int rank, bool split) {
     const int W = p.d_c + p.d_rope;
+    const int eb = p.kv_fp8 ? 1 : 2;  // bytes per cache element
     Geo g;
     if (!split) {
         g.k0 = 0;
@@ -717,19 +992,29 @@ Geo make_geo(const AttnParams &p, int rank, bool split) {
         g.vn = p.d_c - 256;
     }
     g.nbox = (g.kw + 63) / 64;
+    g.pitch = (g.kw * eb + 31) / 32 * 32;
+    g.x_u32 = g.k0 * eb / 4;
     return g;
 }
 
-template <bool kSplit, bool kPaged, bool kSparse>
-cudaError_t launch_variant(const CUtensorMap &tm, const AttnParams &p, const Geo &g0, const Geo &g1, cudaStream_t st) {
+template <bool kSplit, bool kPaged, bool kSparse, bool kFp8>
+cudaError_t launch_variant(const CUtensorMap &tm0, const CUtensorMap &tm1, const AttnParams &p, const Geo &g0,
+                           const Geo &g1, cudaStream_t st) {
+    constexpr bool kStaged = kFp8;
     const int smem = (int)sizeof(Smem) + 1024;
-    auto kern = attn_tc<kSplit, kPaged, kSparse>;
+    auto kern = attn_tc<kSplit, kPaged, kSparse, kFp8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (threads_of(kSparse, kFp8) == 512) {
+        // the register split hands out exactly the registers of a 128-per-thread
+        // launch; with any other allocation the kernel is not run
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != 128) return cudaErrorNotSupported;
+    }
     const int row_blocks = (p.s_q * p.H + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(row_blocks * (kSplit ? 2 : 1), p.num_splits, p.B);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads_of(kSparse, kFp8));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -739,13 +1024,52 @@ cudaError_t launch_variant(const CUtensorMap &tm, const AttnParams &p, const Geo
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tm, p, g0, g1);
+    return cudaLaunchKernelEx(&cfg, kern, tm0, tm1, p, g0, g1);
 }
 
-template <bool kSplit, bool kSparse>
-cudaError_t launch_paged(const CUtensorMap &tm, const AttnParams &p, const Geo &g0, const Geo &g1, cudaStream_t st) {
-    return p.block_table ? launch_variant<kSplit, true, kSparse>(tm, p, g0, g1, st)
-                         : launch_variant<kSplit, false, kSparse>(tm, p, g0, g1, st);
+template <bool kSplit, bool kSparse, bool kFp8>
+cudaError_t launch_paged(const CUtensorMap &tm0, const CUtensorMap &tm1, const AttnParams &p, const Geo &g0,
+                         const Geo &g1, cudaStream_t st) {
+    return p.block_table ? launch_variant<kSplit, true, kSparse, kFp8>(tm0, tm1, p, g0, g1, st)
+                         : launch_variant<kSplit, false, kSparse, kFp8>(tm0, tm1, p, g0, g1, st);
+}
+
+template <bool kSplit>
+cudaError_t launch_split(const CUtensorMap &tm0, const CUtensorMap &tm1, const AttnParams &p, const Geo &g0,
+                         const Geo &g1, cudaStream_t st) {
+    const bool sparse = p.indices != nullptr;
+    if (p.kv_fp8)
+        return sparse ? launch_paged<kSplit, true, true>(tm0, tm1, p, g0, g1, st)
+                      : launch_paged<kSplit, false, true>(tm0, tm1, p, g0, g1, st);
+    return sparse ? launch_paged<kSplit, true, false>(tm0, tm1, p, g0, g1, st)
+                  : launch_paged<kSplit, false, false>(tm0, tm1, p, g0, g1, st);
+}
+
+// Tensor map of the FP8 variants for one CTA's slice: rows of 32-bit
+// elements, a box of one row (sparse gathers) or of one 64-token tile.
+bool encode_slice_map(CUtensorMap *tm, const AttnParams &p, const Geo &g, bool sparse) {
+    const int W = p.d_c + p.d_rope;
+    const uint64_t eb = p.kv_fp8 ? 1 : 2;
+    const uint64_t row_u32 = (uint64_t)W * eb / 4;
+    const uint32_t box_x = (uint32_t)(g.pitch / 4);
+    if (sparse) {
+        const uint64_t rows = p.block_table ? (uint64_t)p.num_pages * p.page_size
+                                            : (uint64_t)p.B * (uint64_t)(p.seq_stride / W);
+        uint64_t dims[2] = {row_u32, rows};
+        uint64_t strides[1] = {(uint64_t)W * eb};
+        uint32_t box[2] = {box_x, 1};
+        return encode_u32_plain(tm, p.kv, 2, dims, strides, box);
+    }
+    if (p.block_table) {
+        uint64_t dims[2] = {row_u32, (uint64_t)p.num_pages * p.page_size};
+        uint64_t strides[1] = {(uint64_t)W * eb};
+        uint32_t box[2] = {box_x, kTile};
+        return encode_u32_plain(tm, p.kv, 2, dims, strides, box);
+    }
+    uint64_t dims[3] = {row_u32, (uint64_t)p.capacity, (uint64_t)p.B};
+    uint64_t strides[2] = {(uint64_t)W * eb, (uint64_t)p.seq_stride * eb};
+    uint32_t box[3] = {box_x, kTile, 1};
+    return encode_u32_plain(tm, p.kv, 3, dims, strides, box);
 }
 
 }  // namespace
@@ -756,29 +1080,36 @@ cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
     const bool sparse = p.indices != nullptr;
     const Geo g0 = make_geo(p, 0, split), g1 = make_geo(p, 1, split);
     if (g0.nbox > kMaxBoxes || g1.nbox > kMaxBoxes || g0.kw % 16 || g1.kw % 16) return cudaErrorNotSupported;
-    CUtensorMap tm;
-    if (sparse) {
+    CUtensorMap tm0, tm1;
+    if (p.kv_fp8) {
+        // the raw codes sit at the top of a stage: 64 rows of at most half a stage
+        if (kTile * g0.pitch > kStageBytes / 2 || kTile * g1.pitch > kStageBytes / 2) return cudaErrorNotSupported;
+        if (!encode_slice_map(&tm0, p, g0, sparse)) return cudaErrorInvalidValue;
+        if (split && !encode_slice_map(&tm1, p, g1, sparse)) return cudaErrorInvalidValue;
+        if (!split) tm1 = tm0;
+    } else if (sparse) {
         // every cache row of the contiguous cache or the pool, gathered one row per entry
         const uint64_t rows = p.block_table ? (uint64_t)p.num_pages * p.page_size
                                             : (uint64_t)p.B * (uint64_t)(p.seq_stride / W);
         uint64_t dims[2] = {(uint64_t)W, rows};
         uint64_t strides[1] = {(uint64_t)W * 2};
         uint32_t box[2] = {64, 1};
-        if (!encode_bf16_sw128(&tm, p.kv, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!encode_bf16_sw128(&tm0, p.kv, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        tm1 = tm0;
     } else if (p.block_table) {
         uint64_t dims[2] = {(uint64_t)W, (uint64_t)p.num_pages * p.page_size};
         uint64_t strides[1] = {(uint64_t)W * 2};
         uint32_t box[2] = {64, kTile};
-        if (!encode_bf16_sw128(&tm, p.kv, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!encode_bf16_sw128(&tm0, p.kv, 2, dims, strides, box)) return cudaErrorInvalidValue;
+        tm1 = tm0;
     } else {
         uint64_t dims[3] = {(uint64_t)W, (uint64_t)p.capacity, (uint64_t)p.B};
         uint64_t strides[2] = {(uint64_t)W * 2, (uint64_t)p.seq_stride * 2};
         uint32_t box[3] = {64, kTile, 1};
-        if (!encode_bf16_sw128(&tm, p.kv, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!encode_bf16_sw128(&tm0, p.kv, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        tm1 = tm0;
     }
-    cudaError_t e;
-    if (split) e = sparse ? launch_paged<true, true>(tm, p, g0, g1, st) : launch_paged<true, false>(tm, p, g0, g1, st);
-    else e = sparse ? launch_paged<false, true>(tm, p, g0, g1, st) : launch_paged<false, false>(tm, p, g0, g1, st);
+    cudaError_t e = split ? launch_split<true>(tm0, tm1, p, g0, g1, st) : launch_split<false>(tm0, tm1, p, g0, g1, st);
     if (e != cudaSuccess || p.num_splits == 1) return e;
     return launch_attn_combine(p, st);
 }

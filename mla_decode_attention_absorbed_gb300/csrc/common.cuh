@@ -14,7 +14,9 @@ struct AttnParams {
     int B, H, s_q, d_c, d_rope;
     float scale;
     const __nv_bfloat16 *q_cat;   // [B][s_q][H][W]
-    const __nv_bfloat16 *kv;      // contiguous or pool, rows of W
+    const void *kv;               // contiguous or pool, rows of W elements (bf16, or E4M3 codes)
+    int kv_fp8;                   // 1: E4M3 codes, value = kv_scale * code
+    float kv_scale;
     long long seq_stride;         // contiguous: elements between sequences
     int capacity;                 // tokens a sequence may hold
     const int *block_table;       // NULL => contiguous
@@ -40,13 +42,15 @@ __device__ __forceinline__ bool seq_len_ok(const AttnParams &p, int L) {
     return L >= p.s_q && L <= p.capacity;
 }
 
-// Row of cached token j of sequence b, or nullptr if its page id is out of range.
+// Row of cached token j of sequence b in a bf16 cache, or nullptr if its page
+// id is out of range.
 __device__ __forceinline__ const __nv_bfloat16 *kv_row(const AttnParams &p, int b, int j) {
     const long long W = p.d_c + p.d_rope;
-    if (p.block_table == nullptr) return p.kv + (long long)b * p.seq_stride + (long long)j * W;
+    const __nv_bfloat16 *kv = static_cast<const __nv_bfloat16 *>(p.kv);
+    if (p.block_table == nullptr) return kv + (long long)b * p.seq_stride + (long long)j * W;
     int page = __ldg(p.block_table + (long long)b * p.max_pages + j / p.page_size);
     if (page < 0 || page >= p.num_pages) return nullptr;
-    return p.kv + ((long long)page * p.page_size + j % p.page_size) * W;
+    return kv + ((long long)page * p.page_size + j % p.page_size) * W;
 }
 
 // Token range [t0, t1) of split `split` for a history of L tokens: the

@@ -32,7 +32,12 @@ class Dims(ctypes.Structure):
 class Cache(ctypes.Structure):
     _fields_ = [("kv", ctypes.c_void_p), ("seq_stride", ctypes.c_longlong), ("capacity", ctypes.c_int),
                 ("block_table", ctypes.c_void_p), ("max_pages", ctypes.c_int), ("page_size", ctypes.c_int),
-                ("num_pages", ctypes.c_int), ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int)]
+                ("num_pages", ctypes.c_int), ("seq_lens", ctypes.c_void_p), ("max_seq_len", ctypes.c_int),
+                ("kv_dtype", ctypes.c_int), ("kv_scale", ctypes.c_float)]
+
+
+KV_BF16, KV_E4M3 = 0, 1
+ABI_VERSION = 2
 
 
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_workspace_size",
@@ -129,23 +134,28 @@ class Problem:
 
 
 def make_cache(prob: Problem, kv: torch.Tensor, seq_lens: torch.Tensor, block_table=None,
-               page_size: int = 64, max_seq_len: int = 0) -> Cache:
+               page_size: int = 64, max_seq_len: int = 0, kv_scale: float | None = None) -> Cache:
     """Cache descriptor for a contiguous [B, T_max, W] (any sequence stride) or paged
-    [P, page, W] latent cache already on the device."""
+    [P, page, W] latent cache already on the device: bf16 values, or FP8 E4M3 codes
+    (uint8 or float8_e4m3fn) with their ``kv_scale`` (value = kv_scale * code)."""
     W = prob.d_c + prob.d_rope
-    if kv.dtype != torch.bfloat16 or kv.shape[-1] != W or kv.stride(-1) != 1:
-        raise ValueError("kv must be bf16 with rows of d_c + d_rope contiguous values")
+    fp8 = kv.dtype in (torch.uint8, torch.float8_e4m3fn)
+    if (kv.dtype != torch.bfloat16 and not fp8) or kv.shape[-1] != W or kv.stride(-1) != 1:
+        raise ValueError("kv must be bf16 or FP8 codes with rows of d_c + d_rope contiguous values")
+    if fp8 and kv_scale is None:
+        raise ValueError("an FP8 cache needs its kv_scale")
+    dt, sc = (KV_E4M3, float(kv_scale)) if fp8 else (KV_BF16, 1.0)
     if block_table is None:
         if kv.dim() != 3 or kv.stride(1) != W:
             raise ValueError("contiguous kv must be [B, T_max, W] with dense token rows")
         return Cache(kv.data_ptr(), kv.stride(0), kv.shape[1], None, 0, page_size, 0,
-                     seq_lens.data_ptr(), int(max_seq_len))
+                     seq_lens.data_ptr(), int(max_seq_len), dt, sc)
     if not kv.is_contiguous() or kv.dim() != 3:
         raise ValueError("paged kv must be a dense [P, page, W] pool")
     if block_table.dtype != torch.int32 or not block_table.is_contiguous():
         raise ValueError("block_table must be a dense int32 [B, max_pages] tensor")
     return Cache(kv.data_ptr(), 0, 0, block_table.data_ptr(), block_table.shape[1], kv.shape[1],
-                 kv.shape[0], seq_lens.data_ptr(), int(max_seq_len))
+                 kv.shape[0], seq_lens.data_ptr(), int(max_seq_len), dt, sc)
 
 
 # ---------------------------------------------------------------------------- entry points
@@ -299,11 +309,11 @@ class Decoder:
     absorb_q -> decode_attn -> out_proj on the current stream."""
 
     def __init__(self, prob: Problem, kv, seq_lens, w_uk, w_uv, block_table=None, page_size=64,
-                 max_seq_len=0, num_splits=0):
+                 max_seq_len=0, num_splits=0, kv_scale=None):
         self.prob = prob
         self.kv, self.seq_lens, self.block_table = kv, seq_lens, block_table
         self.w_uk, self.w_uv = w_uk, w_uv
-        self.cache = make_cache(prob, kv, seq_lens, block_table, page_size, max_seq_len)
+        self.cache = make_cache(prob, kv, seq_lens, block_table, page_size, max_seq_len, kv_scale)
         self.num_splits = num_splits
         dev = kv.device
         B, s_q, H = prob.B, prob.s_q, prob.H

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mla_abi_version() == 1
+    assert lib.mla_abi_version() == 2
     for code in range(10):
         assert lib.mla_status_string(code).decode().startswith("MLA_")
     assert lib.mla_status_string(99).decode() == "unknown mla status"
