@@ -71,6 +71,9 @@ def _load():
             lib.orc_threads.restype = ctypes.c_int
             lib.orc_e4m3_to_f64.restype = ctypes.c_double
             lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.orc_f64_to_e4m3.restype = ctypes.c_uint8
+            lib.orc_f64_to_e4m3.argtypes = [ctypes.c_double]
+            lib.orc_encode_e4m3.argtypes = [LL, P, P]
             lib.orc_absorb_q.argtypes = [ctypes.POINTER(_Dims), P, P, P, P]
             lib.orc_attend.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache), P, LL, P, P]
             lib.orc_attend_partial.argtypes = [ctypes.POINTER(_Dims), P, ctypes.POINTER(_Cache),
@@ -170,6 +173,15 @@ def e4m3_to_f64(code: int) -> float:
     return float(_load().orc_e4m3_to_f64(int(code) & 0xFF))
 
 
+def e4m3_encode(values) -> torch.Tensor:
+    """E4M3 codes (uint8) of float64 values: nearest, ties to even, saturating at
+    +-448 (see orc_f64_to_e4m3)."""
+    v = _f64(torch.as_tensor(values))
+    out = torch.empty(v.shape, dtype=torch.uint8)
+    _load().orc_encode_e4m3(int(v.numel()), _ptr(v), _ptr(out))
+    return out
+
+
 def attend(d, q_cat, kv, seq_lens, block_table=None, page_size=64, rows=None, kv_scale=None):
     """(o_lat [B, s_q, H, d_c], lse [B, s_q, H]) float64 from a float64-widened q_cat.
 
@@ -250,7 +262,7 @@ def down_proj(x, w_dkv) -> torch.Tensor:
     return c.view(*x.shape[:-1], d_c)
 
 
-def cache_append(d, x, w_dkv, k_rope, kv, seq_lens, block_table=None, page_size=64):
+def cache_append(d, x, w_dkv, k_rope, kv, seq_lens, block_table=None, page_size=64, kv_scale=None):
     """The cache after appending the new tokens, in fp64, and a bool mask of the
     rows written ("MLA, dim by dim", "MLA Decode": c = x . W_DKV is appended).
 
@@ -258,11 +270,23 @@ def cache_append(d, x, w_dkv, k_rope, kv, seq_lens, block_table=None, page_size=
     position L_b - s_q + i (seq_lens already count the new tokens): row
     [c | k_rope] of the contiguous cache [B, T_max, W], or of page
     block_table[b][pos // page_size] of the pool [P, page_size, W].  Invalid
-    lengths or page ids write nothing."""
+    lengths or page ids write nothing.  For an FP8 cache (uint8 codes with
+    ``kv_scale``) the returned cache holds the exact values divided by kv_scale
+    for the written rows (the codes a quantiser must round) and the old codes'
+    values elsewhere; e4m3_encode turns it into codes."""
     c = down_proj(x, w_dkv)
-    out = kv.detach().to("cpu", torch.float64).clone()
+    fp8 = kv.dtype in (torch.uint8, torch.float8_e4m3fn)
+    if fp8:
+        if kv_scale is None:
+            raise ValueError("an FP8 cache needs its kv_scale")
+        out = kv.detach().to("cpu").contiguous().view(torch.float8_e4m3fn).to(torch.float64)
+        c = c / float(kv_scale)
+    else:
+        out = kv.detach().to("cpu", torch.float64).clone()
     written = torch.zeros(out.shape[:-1], dtype=torch.bool)
     kr = k_rope.detach().to("cpu", torch.float64)
+    if fp8:
+        kr = kr / float(kv_scale)
     lens = [int(v) for v in seq_lens.detach().to("cpu")]
     bt = block_table.detach().to("cpu") if block_table is not None else None
     cap = int(bt.shape[1]) * page_size if bt is not None else int(kv.shape[1])

@@ -84,6 +84,32 @@ double orc_e4m3_to_f64(uint8_t code)
     return s ? -v : v;
 }
 
+/* The E4M3 code nearest to v (ties to the code with an even mantissa, the
+ * nearest-even rule), saturating: beyond the largest finite value 448 the code
+ * of +-448; NaN gives the NaN code 0x7F.  Found by searching the 127 finite
+ * non-negative codes, so it follows the format's definition directly. */
+uint8_t orc_f64_to_e4m3(double v)
+{
+    if (v != v) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(orc_e4m3_to_f64((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+void orc_encode_e4m3(long long n, const double *v, uint8_t *codes)
+{
+    for (long long i = 0; i < n; ++i) codes[i] = orc_f64_to_e4m3(v[i]);
+}
+
 /* Element k of a cached row (bf16 widened, or the scaled FP8 value). */
 static double row_elem(const orc_cache *c, const void *row, long long k)
 {

@@ -585,3 +585,35 @@ def test_fp8_canaries_stay_unread():
     assert bool((codes == 0x7F).any())
     o8, l8 = oracle.attend(cfg, q, codes, inp["seq_lens"], kv_scale=1.0 / 16.0)
     assert not torch.isnan(o8).any() and not torch.isnan(l8).any()
+
+
+def test_e4m3_encode_roundtrip_ties_and_saturation():
+    """Encoding every finite code's value gives the code back; midpoints round to
+    the even code; values past 448 saturate; the library cast agrees in range."""
+    vals = torch.tensor([oracle.e4m3_to_f64(c) for c in range(256)], dtype=torch.float64)
+    codes = oracle.e4m3_encode(vals)
+    fin = ~torch.isnan(vals)
+    idx = torch.arange(256)[fin]
+    back = codes[fin].to(torch.int64)
+    # +0 and -0 both encode to themselves
+    assert torch.equal(back, idx)
+    # midpoints between consecutive positive codes go to the even one
+    for c in range(0, 0x7E):
+        mid = (oracle.e4m3_to_f64(c) + oracle.e4m3_to_f64(c + 1)) / 2
+        assert int(oracle.e4m3_encode([mid])[0]) == (c if c % 2 == 0 else c + 1)
+    assert int(oracle.e4m3_encode([1e6])[0]) == 0x7E and int(oracle.e4m3_encode([-500.0])[0]) == 0xFE
+    x = torch.randn(4000, generator=torch.Generator().manual_seed(5), dtype=torch.float64) * 40
+    assert torch.equal(oracle.e4m3_encode(x), x.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8))
+
+
+def test_fp8_append_rows_are_the_quantised_down_projection():
+    from mla_decode_attention_absorbed_gb300.workloads import to_fp8_cache
+    cfg, inp, a, _, _ = _append_case(paged=False)
+    codes = to_fp8_cache(inp["kv"])
+    out8, w8 = oracle.cache_append(cfg, a["x"], a["w_dkv"], a["k_rope"], codes, inp["seq_lens"], kv_scale=1.0 / 16.0)
+    outb, wb = oracle.cache_append(cfg, a["x"], a["w_dkv"], a["k_rope"], inp["kv"], inp["seq_lens"])
+    assert torch.equal(w8, wb)
+    # written rows: the exact values divided by the scale; others: the old codes' values
+    assert torch.allclose(out8[w8], outb[wb] * 16.0, rtol=0, atol=0)
+    old = codes.view(torch.float8_e4m3fn).to(torch.float64)
+    assert torch.equal(out8[~w8].nan_to_num(1e9), old[~w8].nan_to_num(1e9))
