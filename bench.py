@@ -420,9 +420,13 @@ def main_op(args):
     mla.load()
     c = cfg.with_(seed=replica_seed(cfg.seed, rank))
     inp = make_inputs(c)
+    kv_scale, eb = None, 2
+    if args.kv == "fp8":
+        inp["kv"] = to_fp8_cache(inp["kv"])
+        kv_scale, eb = KV_FP8_SCALE, 1
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     prob = mla.Problem.of(c)
-    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size)
+    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size, kv_scale=kv_scale)
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     pk = peaks()
     assert args.op == "append"
@@ -431,7 +435,7 @@ def main_op(args):
     ws = mla.alloc_workspace(mla.cache_append_workspace_size(prob, D_MODEL), dev)
     M = c.B * c.s_q
     # algorithmic work: every W_DKV, x and k_rope byte read once, the new cache rows written once
-    bytes_ = (D_MODEL * c.d_c + M * D_MODEL + M * c.d_rope + M * c.W) * 2 + c.B * 4
+    bytes_ = (D_MODEL * c.d_c + M * D_MODEL + M * c.d_rope) * 2 + M * c.W * eb + c.B * 4
     flops = 2 * M * D_MODEL * c.d_c
 
     def step():
@@ -478,12 +482,12 @@ def main_op(args):
     flat = flat.to(dev)
     kv_rows = d["kv"].view(-1, c.W)
     gather = lambda: kv_rows.index_select(0, flat)  # noqa: E731
-    h_rows = torch.empty(M, c.W, dtype=torch.bfloat16).pin_memory()
+    h_rows = torch.empty(M, c.W, dtype=d["kv"].dtype).pin_memory()
     e2e_steps = max(3, min(args.steps, 50))
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    rows_dev = torch.empty(M, c.W, dtype=torch.bfloat16, device=dev)
+    rows_dev = torch.empty(M, c.W, dtype=d["kv"].dtype, device=dev)
     for _ in range(e2e_steps):
         a["x"].copy_(h_x, non_blocking=True)
         a["k_rope"].copy_(h_kr, non_blocking=True)
@@ -516,9 +520,10 @@ def main_op(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if args.kv == "bf16" else "bf16 GEMM, e4m3 cache rows",
         "data": "synthetic (seeded N(0,1) hidden states, N(0,1/d_model) W_DKV)",
-        "config": {"workload": f"append to {workload_name(c)}, d_model={D_MODEL}",
+        "config": {"workload": f"append to {workload_name(c)}, d_model={D_MODEL}"
+                               + (", FP8 E4M3 cache (scale 1/16)" if args.kv == "fp8" else ""),
                    "l2": "L2 flushed between steps (256 MB write)",
                    "launch": "the step's kernels replayed as a CUDA graph",
                    "parallelism": f"{world} independent replica(s)"},
@@ -530,7 +535,7 @@ def main_op(args):
                      "tflops": flops / (ms * 1e-3) / 1e12},
         "cpu_baseline": cpu,
         "e2e": {"value": bytes_ * world / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": (h_x.numel() + h_kr.numel()) * 2, "d2h_bytes_per_step": h_rows.numel() * 2,
+                "h2d_bytes_per_step": (h_x.numel() + h_kr.numel()) * 2, "d2h_bytes_per_step": h_rows.numel() * h_rows.element_size(),
                 "note": "pinned host x / k_rope in, the appended cache rows back, every step"},
         "gpu_launches": 2 * args.steps,  # split-K GEMM + scatter (the accumulator memset is a driver op)
         "clocks": clocks.summary(),

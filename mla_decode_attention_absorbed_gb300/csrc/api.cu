@@ -217,7 +217,6 @@ MLA_API int mla_cache_append(const mla_dims *dims, int d_model, const void *x, c
     if (d_model % 8) return MLA_ERR_ALIGN;  // rows of x must be whole 16-byte units
     s = check_cache(dims, cache);
     if (s) return s;
-    if (cache->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     if (ws_bytes < mla_cache_append_workspace_size(dims, d_model)) return MLA_ERR_WORKSPACE;

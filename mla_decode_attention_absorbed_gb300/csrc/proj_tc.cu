@@ -258,6 +258,15 @@ cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void 
 // 8-column chunks, four groups each summing every fourth split, summed through
 // shared memory (the partials' loads are independent, not one chain).
 constexpr int kScatterThreads = 256;
+// Four values as E4M3 codes (value 0 in the low byte): round to nearest even,
+// saturating at +-448.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float v0, float v1, float v2, float v3) {
+    unsigned short lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(v1), "f"(v0));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(v3), "f"(v2));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
 __global__ void __launch_bounds__(kScatterThreads) append_scatter(AttnParams p, const float *part, int splits,
                                                                   const __nv_bfloat16 *k_rope) {
     __shared__ float red[3][512];
@@ -269,12 +278,20 @@ __global__ void __launch_bounds__(kScatterThreads) append_scatter(AttnParams p, 
         if (threadIdx.x == 0) set_status(p.status, MLA_ERR_SEQLEN);
         return;
     }
-    const __nv_bfloat16 *row = kv_row(p, b, L - p.s_q + i);
-    if (row == nullptr) {
-        if (threadIdx.x == 0) set_status(p.status, MLA_ERR_PAGE);
-        return;
+    // the row's element offset in the cache (bf16 values or E4M3 codes)
+    const int pos = L - p.s_q + i;
+    const long long W = p.d_c + p.d_rope;
+    long long at;
+    if (p.block_table == nullptr) {
+        at = (long long)b * p.seq_stride + (long long)pos * W;
+    } else {
+        const int page = __ldg(p.block_table + (long long)b * p.max_pages + pos / p.page_size);
+        if (page < 0 || page >= p.num_pages) {
+            if (threadIdx.x == 0) set_status(p.status, MLA_ERR_PAGE);
+            return;
+        }
+        at = ((long long)page * p.page_size + pos % p.page_size) * W;
     }
-    __nv_bfloat16 *dst = const_cast<__nv_bfloat16 *>(row);
     const int grp = threadIdx.x / 64, c = 8 * (threadIdx.x % 64);  // d_c <= 512: one chunk per thread
     float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (c < p.d_c) {
@@ -289,6 +306,30 @@ __global__ void __launch_bounds__(kScatterThreads) append_scatter(AttnParams p, 
             for (int e = 0; e < 8; ++e) red[grp - 1][c + e] = a[e];
     }
     __syncthreads();
+    if (p.kv_fp8) {
+        // FP8 cache: the code of value / kv_scale for every element, RoPE key included
+        uint8_t *dst = const_cast<uint8_t *>(static_cast<const uint8_t *>(p.kv)) + at;
+        const float s = p.kv_scale;
+        if (grp == 0 && c < p.d_c) {
+            for (int e = 0; e < 8; ++e) a[e] += red[0][c + e] + red[1][c + e] + red[2][c + e];
+            *reinterpret_cast<uint2 *>(dst + c) = make_uint2(pack_e4m3x4(a[0] / s, a[1] / s, a[2] / s, a[3] / s),
+                                                             pack_e4m3x4(a[4] / s, a[5] / s, a[6] / s, a[7] / s));
+        }
+        if (grp == 1 && c < p.d_rope) {
+            const uint4 u = *reinterpret_cast<const uint4 *>(k_rope + (long long)m * p.d_rope + c);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+            float f[8];
+            for (int e = 0; e < 4; ++e) {
+                const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w4[e]));
+                f[2 * e] = v.x / s;
+                f[2 * e + 1] = v.y / s;
+            }
+            *reinterpret_cast<uint2 *>(dst + p.d_c + c) =
+                make_uint2(pack_e4m3x4(f[0], f[1], f[2], f[3]), pack_e4m3x4(f[4], f[5], f[6], f[7]));
+        }
+        return;
+    }
+    __nv_bfloat16 *dst = const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(p.kv)) + at;
     if (grp == 0 && c < p.d_c) {
         for (int e = 0; e < 8; ++e) a[e] += red[0][c + e] + red[1][c + e] + red[2][c + e];
         *reinterpret_cast<uint4 *>(dst + c) = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),

@@ -87,3 +87,47 @@ def test_append_host_errors():
     app = make_append_inputs(cfg, d_model=60)  # not a multiple of 8
     with pytest.raises(mla.MLAError):
         _run(cfg, inp, app)
+
+
+# ------------------------------------------------------------------ FP8 (E4M3) cache
+def _fp8_codes_ok(got, exact):
+    """got: E4M3 codes from the GPU; exact: the float64 values they quantise.  The
+    code must be the nearest one (ties to even, saturating), or -- where the exact
+    value lies within fp32 summation error of the midpoint between two codes --
+    its other neighbour."""
+    ref = oracle.e4m3_encode(exact)
+    same = got == ref
+    if bool(same.all()):
+        return
+    g = got[~same].view(torch.float8_e4m3fn).to(torch.float64)
+    r = ref[~same].view(torch.float8_e4m3fn).to(torch.float64)
+    v = exact[~same]
+    mid = (g + r) / 2
+    # neighbouring codes, and v within 1e-4 relative of their midpoint
+    assert bool(((mid - v).abs() <= 1e-4 * v.abs().clamp(min=1e-3)).all()), (g[:5], r[:5], v[:5])
+    assert bool(((g - r).abs() <= (v.abs() * 2.0 ** -2).clamp(min=2.0 ** -9)).all())
+
+
+@pytest.mark.parametrize("paged,s_q,scale", [(False, 1, 1.0 / 16), (True, 2, 1.0 / 16), (False, 2, 0.0371)])
+def test_append_fp8(paged, s_q, scale):
+    """Appending into an FP8 cache: every element of the new rows is the E4M3 code
+    of value / kv_scale; every other code is unchanged."""
+    from mla_decode_attention_absorbed_gb300.workloads import to_fp8_cache
+    cfg = MLAConfig("append_fp8", B=16, s_q=s_q, len_lo=s_q, len_hi=500, paged=paged, seed=12, **_DSV3)
+    inp = make_inputs(cfg)
+    app = make_append_inputs(cfg, d_model=7168)
+    codes = to_fp8_cache(inp["kv"], scale)
+    dev = "cuda"
+    kv = codes.to(dev).clone()
+    lens = inp["seq_lens"].to(dev)  # the descriptor holds raw pointers: keep the tensors alive
+    bt = inp["block_table"].to(dev) if inp["block_table"] is not None else None
+    prob = mla.Problem.of(cfg)
+    cache = mla.make_cache(prob, kv, lens, bt, cfg.page_size, kv_scale=scale)
+    ws = mla.cache_append(prob, app["x"].to(dev), app["w_dkv"].to(dev), app["k_rope"].to(dev), cache)
+    assert mla.read_status(ws) == 0
+    got = kv.cpu()
+    exact, written = oracle.cache_append(cfg, app["x"], app["w_dkv"], app["k_rope"], codes, inp["seq_lens"],
+                                         inp["block_table"], cfg.page_size, kv_scale=scale)
+    assert int(written.sum()) == cfg.B * s_q
+    assert torch.equal(got[~written], codes[~written])
+    _fp8_codes_ok(got[written], exact[written])
