@@ -337,7 +337,7 @@ def main_ours(args):
         achieved = w["attn_bytes"] / attn_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"]}
-    roof["traffic"] = traffic_for(f"attn:{cfg.name}")
+    roof["traffic"] = traffic_for(f"attn{'_fp8' if args.kv == 'fp8' else ''}:{cfg.name}")
     roof["kernel"] = "mla_decode_attn (split-T attention + LSE combine)" + (
         ", FP8 E4M3 cache dequantised on chip, fp16 MMAs" if args.kv == "fp8" else "")
     roof["peak_source"] = pk["source"] + (" burst bf16" if tensor_bound else " HBM copy")
@@ -676,7 +676,8 @@ def main_sparse(args, cfg, rank, world, local, active):
     else:
         ach = attn_bytes / attn_s / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": ach / pk["hbm_gbs"]}
-    roof.update({"traffic": None, "kernel": "mla_decode_attn_sparse (gathered top-k attention)",
+    roof.update({"traffic": traffic_for(f"attn_sparse{'_fp8' if args.kv == 'fp8' else ''}:{cfg.name}"),
+                 "kernel": "mla_decode_attn_sparse (gathered top-k attention)",
                  "peak_source": pk["source"] + (" burst bf16" if tensor_bound else " HBM copy"),
                  "roofline_time_us": max(attn_flops / (pk["bf16_tflops"] * 1e12),
                                          attn_bytes / (pk["hbm_gbs"] * 1e9)) * 1e6,
