@@ -16,6 +16,10 @@
  *                    per query token (sparse top-k decode)
  *   mla_cache_append c_kv = x . W_DKV of the new tokens, written with their
  *                    (already rotated) RoPE keys into the latent cache
+ *   mla_prefill      prefill / chunked prefill of s_q new tokens: the absorbed path above
+ *                    below the crossover S*, the expand form (per-head K, V
+ *                    re-expanded from the latent, then per-head attention) at or
+ *                    above it ("Why MLA and MTP Fight Each Other", 5.5-5.8)
  *   mla_naive_decode the decompress-then-attend form, a comparison point only
  *                    ("The MLA decode speedup hiding in your model card",
  *                    section "The naive form, written out")
@@ -40,7 +44,8 @@
  *    and nothing reads outside the caller's buffers.
  *  - Dimensions: H >= 1, s_q >= 1, d_c a multiple of 64 up to 512, d_rope a
  *    multiple of 16 up to 64, d_nope and d_v multiples of 16 from 16 to 256,
- *    s_q * H <= 4096.  Other shapes return MLA_ERR_UNSUPPORTED.
+ *    s_q * H <= 65536 (the prefill entry points: s_q <= 2^20 on the expand
+ *    path).  Other shapes return MLA_ERR_UNSUPPORTED.
  */
 #ifndef MLA_H
 #define MLA_H
@@ -262,6 +267,55 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
 MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
                                     void *o_lat, float *lse, int num_splits, int *device_status,
                                     void *stream);
+
+/* Which path mla_prefill took. */
+typedef enum { MLA_PATH_ABSORB = 0, MLA_PATH_EXPAND = 1 } mla_path;
+
+/* The query count S* at which the absorbed and the expanded bracketings of one
+ * layer cost the same FLOPs for a history of L cached tokens ("Why MLA and MTP
+ * Fight Each Other", 5.3 and 5.6; H cancels):
+ *   S* = L d_c (d_nope + d_v) / (d_c (d_nope + d_v) + L (2 d_c - d_nope - d_v)),
+ * 128 at L = 512 rising to 171 at L = 128K for DeepSeek-V3 widths.  Host only;
+ * returns 0 for invalid dims or L < 1. */
+MLA_API double mla_prefill_crossover(const mla_dims *dims, long long L);
+
+/* Bytes of workspace mla_prefill_expand needs: the status word, the queries
+ * [q_nope | q_rope] (B*s_q*H*(d_nope+d_rope) bf16) and the expanded rows
+ * (B*H*capacity*(d_v+d_nope+d_rope) bf16: 671 MB for one 8K-token sequence at
+ * DeepSeek-V3 widths).  0 for invalid arguments or an unsupported shape. */
+MLA_API size_t mla_prefill_expand_workspace_size(const mla_dims *dims, const mla_cache *cache);
+
+/* Prefill in the expand form ("Why MLA and MTP Fight Each Other", 5.5: with
+ * many query tokens the per-token expansion is amortised; "MLA, dim by dim",
+ * MLA prefill: materialise K and V from the latent, then standard attention):
+ *   K_h[j] = c_kv[j] . W_UK[h],  V_h[j] = c_kv[j] . W_UV[h]       for every cached j < L_b
+ *   s_ij = scale * (q_nope[i,h] . K_h[j] + q_rope[i,h] . k_rope[j]),  j <= L_b - s_q + i
+ *   out[b,i,h,:] = sum_j softmax_j(s_ij) V_h[j],  lse[b,i,h] = log sum_j exp(s_ij)
+ * Inputs as mla_naive_decode (q_nope [B][s_q][H][d_nope], q_rope [B][s_q][H][d_rope],
+ * W_UK [H][d_c][d_nope], W_UV [H][d_c][d_v], a bf16 cache); out bf16
+ * [B][s_q][H][d_v], lse fp32 [B][s_q][H].  The same numbers as the absorbed path
+ * (which equals it in exact arithmetic), computed with tensor-core GEMMs for the
+ * expansion and per-head attention over 64-token tiles.  Requires d_v and
+ * d_nope multiples of 64 with d_v + d_nope <= 256 and d_v + d_nope + d_rope <=
+ * 320, and a bf16 cache; else MLA_ERR_UNSUPPORTED. */
+MLA_API int mla_prefill_expand(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+                               const void *w_uk, const void *w_uv, void *out, float *lse, void *workspace,
+                               size_t ws_bytes, void *stream);
+
+/* Bytes of workspace mla_prefill needs (enough for either path). */
+MLA_API size_t mla_prefill_workspace_size(const mla_dims *dims, const mla_cache *cache);
+
+/* Prefill or chunked prefill of s_q new tokens per sequence, dispatched on the
+ * crossover ("Why MLA and MTP Fight Each Other", 5.6 and 5.8): with L the
+ * longest history (cache->max_seq_len, else the capacity), s_q >= S*(L) takes
+ * mla_prefill_expand, s_q below it (decode, verification) the absorbed path
+ * mla_absorb_q -> mla_decode_attn -> mla_out_proj; shapes the expand form does
+ * not support always take the absorbed path.  Same inputs and outputs as
+ * mla_prefill_expand; *path (optional) receives the mla_path taken.  The
+ * status word is at the start of the workspace for both paths. */
+MLA_API int mla_prefill(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+                        const void *w_uk, const void *w_uv, void *out, float *lse, void *workspace, size_t ws_bytes,
+                        int *path, void *stream);
 
 /* Wait for `stream`, then copy the device status word at the start of
  * `workspace` (written by the last mla_decode_attn / mla_naive_decode that used

@@ -1,5 +1,6 @@
 // C ABI of the MLA decode library: argument checks, workspace layout, launches.
 // Declarations and the contract live in include/mla.h.
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -17,7 +18,8 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int check_dims(const mla_dims *d) {
+// Shapes every entry point supports (the absorbed kernels add a row limit).
+int check_shape(const mla_dims *d) {
     if (!d) return MLA_ERR_NULL;
     if (d->B < 0 || d->H < 1 || d->s_q < 1 || d->d_c < 1 || d->d_rope < 0 || d->d_nope < 1 || d->d_v < 1)
         return MLA_ERR_SHAPE;
@@ -25,8 +27,15 @@ int check_dims(const mla_dims *d) {
     if (d->d_rope % 16 || d->d_rope > 64) return MLA_ERR_UNSUPPORTED;
     if (d->d_nope % 16 || d->d_nope > 256) return MLA_ERR_UNSUPPORTED;
     if (d->d_v % 16 || d->d_v > 256) return MLA_ERR_UNSUPPORTED;
-    if ((long long)d->s_q * d->H > 4096) return MLA_ERR_UNSUPPORTED;
+    if (d->s_q > (1 << 20)) return MLA_ERR_UNSUPPORTED;
     if (!(d->scale == d->scale)) return MLA_ERR_SHAPE;  // NaN scale
+    return MLA_OK;
+}
+
+int check_dims(const mla_dims *d) {
+    const int s = check_shape(d);
+    if (s) return s;
+    if ((long long)d->s_q * d->H > 65536) return MLA_ERR_UNSUPPORTED;
     return MLA_OK;
 }
 
@@ -35,7 +44,7 @@ long long cache_capacity(const mla_cache *c) {
     return c->block_table ? (long long)c->max_pages * c->page_size : (long long)c->capacity;
 }
 
-int check_cache(const mla_dims *d, const mla_cache *c) {
+int check_cache(const mla_dims *d, const mla_cache *c) {  // d already passed check_shape
     if (!c) return MLA_ERR_NULL;
     if (d->B == 0) return MLA_OK;
     if (!c->kv || !c->seq_lens) return MLA_ERR_NULL;
@@ -106,6 +115,33 @@ size_t attn_workspace_bytes(const mla_dims *d, int splits) {
 }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// ---------------------------------------------------------------- prefill (expand form)
+// Expanded row width: [V_h (d_v) | K_h (d_nope) | k_rope (d_rope)].
+long long expanded_width(const mla_dims *d) { return (long long)d->d_v + d->d_nope + d->d_rope; }
+
+int check_expand(const mla_dims *d, const mla_cache *c) {
+    if (c->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
+    if (d->d_v % 64 || d->d_nope % 64 || d->d_v + d->d_nope > 256 || expanded_width(d) > 320) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+size_t expand_q_bytes(const mla_dims *d) {
+    return round_up((size_t)d->B * d->s_q * d->H * (d->d_nope + d->d_rope) * 2, 256);
+}
+
+size_t expand_workspace_bytes(const mla_dims *d, const mla_cache *c) {
+    return kStatusBytes + expand_q_bytes(d) +
+           (size_t)d->B * d->H * (size_t)cache_capacity(c) * (size_t)expanded_width(d) * 2;
+}
+
+// absorbed prefill: the attention's own workspace first (so that the status word
+// sits at the start, as for every entry point), then q_cat and o_lat
+size_t absorbed_workspace_bytes(const mla_dims *d, int splits) {
+    const size_t rows = (size_t)d->B * d->s_q * d->H;
+    return round_up(attn_workspace_bytes(d, splits), 256) + round_up(rows * (d->d_c + d->d_rope) * 2, 256) +
+           rows * d->d_c * 2;
+}
 
 mla::AttnParams make_params(const mla_dims *d, const mla_cache *c) {
     mla::AttnParams p;
@@ -320,6 +356,107 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
     char *kbuf = (char *)workspace + kStatusBytes;
     cudaError_t e = mla::launch_naive(p, dims->d_nope, dims->d_v, q_nope, q_rope, w_uk, w_uv, out, lse, kbuf, st);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API double mla_prefill_crossover(const mla_dims *dims, long long L) {
+    if (check_shape(dims) || L < 1) return 0.0;
+    // "Why MLA and MTP Fight Each Other", 5.3 and 5.6: both bracketings cost
+    //   absorb: S * [2 d_c (d_k + d_v) + L (4 d_c)]           (per head, MACs x 2)
+    //   expand: L * 2 d_c (d_k + d_v) + S * L * 2 (d_k + d_v)
+    // and they tie at S* = L d_c (d_k + d_v) / (d_c (d_k + d_v) + L (2 d_c - d_k - d_v)).
+    const double dc = dims->d_c, dk = dims->d_nope, dv = dims->d_v, l = (double)L;
+    const double denom = dc * (dk + dv) + l * (2.0 * dc - dk - dv);
+    return denom > 0.0 ? l * dc * (dk + dv) / denom : INFINITY;
+}
+
+MLA_API size_t mla_prefill_expand_workspace_size(const mla_dims *dims, const mla_cache *cache) {
+    if (check_shape(dims) || check_cache(dims, cache) || check_expand(dims, cache)) return 0;
+    return expand_workspace_bytes(dims, cache);
+}
+
+MLA_API int mla_prefill_expand(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+                               const void *w_uk, const void *w_uv, void *out, float *lse, void *workspace,
+                               size_t ws_bytes, void *stream) {
+    int s = check_shape(dims);
+    if (s) return s;
+    if (!cache) return MLA_ERR_NULL;
+    if ((s = check_cache(dims, cache))) return s;
+    if ((s = check_expand(dims, cache))) return s;
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    if (ws_bytes < expand_workspace_bytes(dims, cache)) return MLA_ERR_WORKSPACE;
+    if (dims->B > 0) {
+        if (!q_nope || !w_uk || !w_uv || !out || !lse || (dims->d_rope && !q_rope)) return MLA_ERR_NULL;
+        if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(out) || !aligned16(lse) ||
+            (q_rope && !aligned16(q_rope)))
+            return MLA_ERR_ALIGN;
+    }
+    cudaStream_t st = as_stream(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dims->B == 0) return MLA_OK;
+    char *base = (char *)workspace + kStatusBytes;
+    void *q_exp = base;
+    void *expd = base + expand_q_bytes(dims);
+    mla::AttnParams p = make_params(dims, cache);
+    p.status = (int *)workspace;
+    cudaError_t e = mla::launch_expand_kv(p, dims->d_nope, dims->d_v, w_uk, w_uv, expd, st);
+    if (e == cudaSuccess) e = mla::launch_concat_q(*dims, q_nope, q_rope, q_exp, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    // per-head attention: (sequence, head) pairs over the expanded rows
+    mla::AttnParams a = p;
+    a.B = dims->B * dims->H;
+    a.H = 1;
+    a.d_c = dims->d_v;
+    a.d_rope = dims->d_nope + dims->d_rope;
+    a.kv = expd;
+    a.block_table = nullptr;
+    a.capacity = (int)cache_capacity(cache);
+    a.seq_stride = (long long)a.capacity * expanded_width(dims);
+    a.q_cat = (const __nv_bfloat16 *)q_exp;
+    a.q_w = dims->d_nope + dims->d_rope;
+    a.heads_per_seq = dims->H;
+    a.o_lat = (__nv_bfloat16 *)out;
+    a.lse = lse;
+    a.num_splits = 1;
+    e = mla::launch_attn_expand(a, st);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API size_t mla_prefill_workspace_size(const mla_dims *dims, const mla_cache *cache) {
+    if (check_shape(dims) || check_cache(dims, cache)) return 0;
+    size_t n = check_dims(dims) ? 0 : absorbed_workspace_bytes(dims, plan_splits(dims, cache, 0));
+    if (!check_expand(dims, cache)) {
+        const size_t e = expand_workspace_bytes(dims, cache);
+        if (e > n) n = e;
+    }
+    return n;
+}
+
+MLA_API int mla_prefill(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+                        const void *w_uk, const void *w_uv, void *out, float *lse, void *workspace, size_t ws_bytes,
+                        int *path, void *stream) {
+    int s = check_shape(dims);
+    if (s) return s;
+    if (!cache) return MLA_ERR_NULL;
+    if ((s = check_cache(dims, cache))) return s;
+    const long long L = cache->max_seq_len > 0 ? cache->max_seq_len : cache_capacity(cache);
+    const bool expand = !check_expand(dims, cache) && (double)dims->s_q >= mla_prefill_crossover(dims, L);
+    if (path) *path = expand ? MLA_PATH_EXPAND : MLA_PATH_ABSORB;
+    if (expand) return mla_prefill_expand(dims, q_nope, q_rope, cache, w_uk, w_uv, out, lse, workspace, ws_bytes, stream);
+    if ((s = check_dims(dims))) return s;
+    const int splits = plan_splits(dims, cache, 0);
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    if (ws_bytes < absorbed_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    const size_t rows = (size_t)dims->B * dims->s_q * dims->H;
+    char *attn_ws = (char *)workspace;
+    char *q_cat = attn_ws + round_up(attn_workspace_bytes(dims, splits), 256);
+    char *o_lat = q_cat + round_up(rows * (dims->d_c + dims->d_rope) * 2, 256);
+    if ((s = mla_absorb_q(dims, q_nope, q_rope, w_uk, q_cat, stream))) return s;
+    if ((s = mla_decode_attn(dims, q_cat, cache, o_lat, lse, attn_ws, attn_workspace_bytes(dims, splits), splits,
+                             stream)))
+        return s;
+    return mla_out_proj(dims, o_lat, w_uv, out, stream);
 }
 
 MLA_API int mla_read_status(const void *workspace, int *status, void *stream) {

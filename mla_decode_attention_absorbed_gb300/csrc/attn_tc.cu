@@ -121,6 +121,9 @@ struct Geo {
     int vn;      // latent columns this CTA accumulates (multiple of 64, <= 256)
     int pitch;   // FP8: bytes of one raw row (the slice, rounded up to 32 B)
     int x_u32;   // FP8: first 32-bit element of the slice within a cache row
+    int sk0;     // first channel of the score contraction, counted from k0 (a multiple of 64)
+    int sw;      // score contraction width (multiple of 16; = kw unless the row carries values apart)
+    int qk0;     // first channel of this CTA's query slice within a q_cat row
 };
 
 struct Smem {
@@ -291,8 +294,12 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     const int rb = kSplit ? blockIdx.x / 2 : blockIdx.x;
     const int split = blockIdx.y, b = blockIdx.z;
     const int rows_total = p.s_q * p.H;
+    // expanded attention: work-item sequence b is head hsub of sequence bseq
+    const int hps = p.heads_per_seq > 1 ? p.heads_per_seq : 1;
+    const int bseq = b / hps, hsub = b % hps;
+    auto row_index = [&](int gr) -> long long { return ((long long)bseq * rows_total + gr) * hps + hsub; };
 
-    const int L = __ldg(p.seq_lens + b);
+    const int L = __ldg(p.seq_lens + bseq);
     const bool seq_ok = seq_len_ok(p, L);
     // [t0, t1): token positions (dense) or positions in the sparse list
     int t0 = 0, t1 = 0;
@@ -497,7 +504,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             // descriptors of stage 0; a stage's are 16-byte-unit offsets of these
             const uint64_t qk_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
             const uint64_t pv_desc0 = smem_desc_sw128(smem_u32(sm.kv[0]), kBoxBytes, 1024);
-            const int nks = g.kw / 16;
+            const int nks = g.sw / 16;
             bool ok = ntiles == 0 || warp_wait(sm, &sm.q_ready, 0);
             for (int n = 0; ok && n < ntiles; ++n) {
                 const int s = n % kRing;
@@ -524,7 +531,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                     if (lane == 0) {
                         // fully unrolled: each MMA is an immediate add to the descriptor and
                         // the A address
-                        const uint64_t db = qk_desc0 + (uint64_t)((s * kStageBytes) >> 4);
+                        const uint64_t db = qk_desc0 + (uint64_t)((s * kStageBytes + (g.sk0 >> 6) * kBoxBytes) >> 4);
                         const uint32_t d_s = tmem + kColS, a_q = tmem + kColQ;
     #pragma unroll
                         for (int ks = 0; ks < kMaxBoxes * 4; ++ks)
@@ -705,14 +712,15 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         // log2 units directly; the two warps of a quadrant take alternate
         // 32-channel chunks; padding rows and channels are zero
         {
-            const __nv_bfloat16 *qrow = p.q_cat + ((long long)b * rows_total + gr) * W;
-            for (int c0 = 32 * hf; c0 < g.kw; c0 += 64) {
+            const int QW = p.q_w > 0 ? p.q_w : W;
+            const __nv_bfloat16 *qrow = p.q_cat + row_index(gr) * QW;
+            for (int c0 = 32 * hf; c0 < g.sw; c0 += 64) {
                 uint32_t v[16];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     uint4 u = make_uint4(0, 0, 0, 0);
-                    const int ch = g.k0 + c0 + e * 8;
-                    if (row_ok && ch < W && c0 + e * 8 < g.kw) u = *reinterpret_cast<const uint4 *>(qrow + ch);
+                    const int ch = g.qk0 + c0 + e * 8;
+                    if (row_ok && ch < QW && c0 + e * 8 < g.sw) u = *reinterpret_cast<const uint4 *>(qrow + ch);
                     const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -918,7 +926,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         const float vscale = kFp8 ? p.kv_scale : 1.f;
         if (p.num_splits == 1) {
             const float inv = any ? vscale / l_row : 0.f;
-            __nv_bfloat16 *dst = p.o_lat + ((long long)b * rows_total + gr) * p.d_c + g.k0;
+            __nv_bfloat16 *dst = p.o_lat + row_index(gr) * p.d_c + g.k0;
             for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
                 tmem_ld16(tmem + lane_base + kColO + c, u);
@@ -935,7 +943,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                 }
             }
             if (store && rank == 0 && hf == 0)
-                p.lse[(long long)b * rows_total + gr] = any ? (m2 + __log2f(l_row)) * ln2 : -INFINITY;
+                p.lse[row_index(gr)] = any ? (m2 + __log2f(l_row)) * ln2 : -INFINITY;
         } else {
             const long long prow = ((long long)b * p.num_splits + split) * rows_total + gr;
             float *dst = p.part_acc + prow * p.d_c + g.k0;
@@ -994,6 +1002,9 @@ Geo make_geo(const AttnParams &p, int rank, bool split) {
     g.nbox = (g.kw + 63) / 64;
     g.pitch = (g.kw * eb + 31) / 32 * 32;
     g.x_u32 = g.k0 * eb / 4;
+    g.sk0 = 0;
+    g.sw = g.kw;
+    g.qk0 = g.k0;
     return g;
 }
 
@@ -1073,6 +1084,34 @@ bool encode_slice_map(CUtensorMap *tm, const AttnParams &p, const Geo &g, bool s
 }
 
 }  // namespace
+
+// Per-head attention over an expanded buffer (the prefill "expand" form): p.kv
+// holds, for each (sequence, head) pair b' = b * heads_per_seq + h, capacity rows
+// [V_h (d_c = d_v) | K_h (d_nope) | k_rope (d_rope_cache)] of W = p.d_c + p.d_rope
+// elements; the score contracts q row [q_nope | q_rope] (p.q_w = d_nope + d_rope
+// elements) with the row's channels [d_v, W), the sum runs over [0, d_v).  One
+// CTA per (128 query tokens, head, sequence), no history split.
+cudaError_t launch_attn_expand(const AttnParams &p, cudaStream_t st) {
+    const int W = p.d_c + p.d_rope;
+    if (p.num_splits != 1 || p.block_table != nullptr || p.indices != nullptr || p.kv_fp8) return cudaErrorNotSupported;
+    if (p.d_c % 64 || p.d_c > 256 || W > kMaxBoxes * 64 || p.q_w != W - p.d_c || p.q_w % 16) return cudaErrorNotSupported;
+    Geo g;
+    g.k0 = 0;
+    g.kw = W;
+    g.vn = p.d_c;
+    g.nbox = (W + 63) / 64;
+    g.pitch = 0;
+    g.x_u32 = 0;
+    g.sk0 = p.d_c;
+    g.sw = p.q_w;
+    g.qk0 = 0;
+    CUtensorMap tm;
+    uint64_t dims[3] = {(uint64_t)W, (uint64_t)p.capacity, (uint64_t)p.B};
+    uint64_t strides[2] = {(uint64_t)W * 2, (uint64_t)p.seq_stride * 2};
+    uint32_t box[3] = {64, kTile, 1};
+    if (!encode_bf16_sw128(&tm, p.kv, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    return launch_variant<false, false, false, false>(tm, tm, p, g, g, st);
+}
 
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
     const int W = p.d_c + p.d_rope;

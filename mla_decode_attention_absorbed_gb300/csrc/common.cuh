@@ -30,6 +30,11 @@ struct AttnParams {
     int *status;                  // device status word
     const int *indices;           // sparse: [B][s_q][topk] token positions (NULL => dense)
     int topk;
+    // expanded (per-head) attention: the B "sequences" are (sequence, head) pairs
+    // b = seq * heads_per_seq + head; lengths are read at seq_lens[seq] and the
+    // query / output / lse rows are [seq][s_q][heads_per_seq] (0 or 1: plain)
+    int heads_per_seq;
+    int q_w;                      // elements per q_cat row (0: d_c + d_rope)
 };
 
 // Record the first device-side error; later ones keep the first.

@@ -26,6 +26,14 @@ inline AppendPlan append_plan(int M, int d_c, int d_model) {
 cudaError_t launch_cache_append_tc(const AttnParams &p, int d_model, const void *x, const void *w_dkv,
                                    const void *k_rope, float *part, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
+cudaError_t launch_attn_expand(const AttnParams &p, cudaStream_t st);
+// Expanded rows [V_h | K_h | k_rope] of every cached token < seq_lens[b] of every
+// sequence and head (the prefill "expand" form), into exp [B][H][capacity][W_e].
+cudaError_t launch_expand_kv(const AttnParams &p, int d_nope, int d_v, const void *w_uk, const void *w_uv, void *exp,
+                             cudaStream_t st);
+// q_exp [B][s_q][H][d_nope + d_rope] = [q_nope | q_rope]
+cudaError_t launch_concat_q(const mla_dims &d, const void *q_nope, const void *q_rope, void *q_exp, cudaStream_t st);
+
 cudaError_t launch_attn_combine(const AttnParams &p, cudaStream_t st);
 cudaError_t launch_naive(const AttnParams &p, int d_nope, int d_v, const void *q_nope, const void *q_rope,
                          const void *w_uk, const void *w_uv, void *out, float *lse, void *kv_scratch,

@@ -43,7 +43,9 @@ ABI_VERSION = 2
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_workspace_size",
            "mla_decode_num_splits", "mla_decode_attn", "mla_out_proj", "mla_naive_workspace_size",
            "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc", "mla_cache_append_workspace_size",
-           "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse")
+           "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse", "mla_prefill_crossover",
+           "mla_prefill_expand_workspace_size", "mla_prefill_expand", "mla_prefill_workspace_size", "mla_prefill")
+PATH_ABSORB, PATH_EXPAND = 0, 1
 
 
 def lib_path() -> str:
@@ -88,6 +90,16 @@ def load(path: str | None = None):
     lib.mla_cache_append.restype = I
     lib.mla_read_status.argtypes = [P, ctypes.POINTER(I), P]
     lib.mla_read_status.restype = I
+    lib.mla_prefill_crossover.argtypes = [pd, ctypes.c_longlong]
+    lib.mla_prefill_crossover.restype = ctypes.c_double
+    lib.mla_prefill_expand_workspace_size.argtypes = [pd, pc]
+    lib.mla_prefill_expand_workspace_size.restype = SZ
+    lib.mla_prefill_expand.argtypes = [pd, P, P, pc, P, P, P, P, P, SZ, P]
+    lib.mla_prefill_expand.restype = I
+    lib.mla_prefill_workspace_size.argtypes = [pd, pc]
+    lib.mla_prefill_workspace_size.restype = SZ
+    lib.mla_prefill.argtypes = [pd, P, P, pc, P, P, P, P, P, SZ, ctypes.POINTER(I), P]
+    lib.mla_prefill.restype = I
     lib.mla_decode_attn_noalloc.argtypes = [pd, P, pc, P, P, I, P, P]
     lib.mla_decode_attn_noalloc.restype = I
     if path is None:
@@ -285,6 +297,56 @@ def naive_decode(prob: Problem, q_nope, q_rope, cache: Cache, w_uk, w_uv, out=No
                                 _ptr(w_uv), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                 _stream(stream)), "mla_naive_decode")
     return out, lse, workspace
+
+
+def prefill_crossover(prob: Problem, L: int) -> float:
+    """mla_prefill_crossover: the query count S* where both bracketings tie (host only)."""
+    d = prob.dims()
+    return float(load().mla_prefill_crossover(ctypes.byref(d), int(L)))
+
+
+def _prefill_outputs(prob, dev, out, lse):
+    if out is None:
+        out = torch.empty(prob.B, prob.s_q, prob.H, prob.d_v, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(prob.B, prob.s_q, prob.H, dtype=torch.float32, device=dev)
+    return out, lse
+
+
+def prefill_expand(prob: Problem, q_nope, q_rope, cache: Cache, w_uk, w_uv, out=None, lse=None, workspace=None,
+                   stream=None):
+    """mla_prefill_expand: K, V re-expanded per head, then per-head attention."""
+    lib = load()
+    out, lse = _prefill_outputs(prob, q_nope.device, out, lse)
+    d = prob.dims()
+    if workspace is None:
+        n = lib.mla_prefill_expand_workspace_size(ctypes.byref(d), ctypes.byref(cache))
+        if n == 0:
+            raise ValueError("mla_prefill_expand_workspace_size rejected the arguments")
+        workspace = alloc_workspace(n, q_nope.device)
+    _check(lib.mla_prefill_expand(ctypes.byref(d), _ptr(q_nope), _ptr(q_rope), ctypes.byref(cache), _ptr(w_uk),
+                                  _ptr(w_uv), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "mla_prefill_expand")
+    return out, lse, workspace
+
+
+def prefill(prob: Problem, q_nope, q_rope, cache: Cache, w_uk, w_uv, out=None, lse=None, workspace=None,
+            stream=None):
+    """mla_prefill: absorbed below the crossover S*, expanded at or above it.
+    Returns (out, lse, workspace, path)."""
+    lib = load()
+    out, lse = _prefill_outputs(prob, q_nope.device, out, lse)
+    d = prob.dims()
+    if workspace is None:
+        n = lib.mla_prefill_workspace_size(ctypes.byref(d), ctypes.byref(cache))
+        if n == 0:
+            raise ValueError("mla_prefill_workspace_size rejected the arguments")
+        workspace = alloc_workspace(n, q_nope.device)
+    path = ctypes.c_int(-1)
+    _check(lib.mla_prefill(ctypes.byref(d), _ptr(q_nope), _ptr(q_rope), ctypes.byref(cache), _ptr(w_uk), _ptr(w_uv),
+                           _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), ctypes.byref(path),
+                           _stream(stream)), "mla_prefill")
+    return out, lse, workspace, int(path.value)
 
 
 def decode_attn_noalloc(prob: Problem, q_cat, cache: Cache, o_lat, lse, num_splits: int = 0,

@@ -65,7 +65,7 @@ def test_host_validation_without_gpu(lib):
     # misaligned pointer
     assert lib.mla_absorb_q(ctypes.byref(d), ctypes.c_void_p(0x40008), a, a, a, nul) == 4
     # unsupported shapes
-    for bad in (dict(d_c=96), dict(d_c=1024), dict(d_rope=8), dict(d_nope=24), dict(d_v=512), dict(H=4097)):
+    for bad in (dict(d_c=96), dict(d_c=1024), dict(d_rope=8), dict(d_nope=24), dict(d_v=512), dict(H=65537)):
         p = dsv3()
         for k, v in bad.items():
             setattr(p, k, v)
@@ -101,3 +101,14 @@ def test_workspace_and_split_queries(lib):
     assert lib.mla_decode_workspace_size(None, None, 0) == 0
     naive = lib.mla_naive_workspace_size(ctypes.byref(d), ctypes.byref(fake_cache(4096)))
     assert naive >= 64 * 128 * 4096 * 256 * 2
+
+
+def test_prefill_crossover_matches_the_pages_formula(lib):
+    """The library's dispatch point (host code) against the oracle's counter, which
+    the page figures pin (S* = 128 at L = 512, 170 at 32K, 171 at 128K)."""
+    from oracle import counts
+    prob = mla.Problem(B=1, H=128, s_q=1, d_c=512, d_rope=64, d_nope=128, d_v=128, scale=1.0)
+    for L in (512, 4096, 32768, 131072):
+        assert abs(mla.prefill_crossover(prob, L) - counts.crossover_S(512, 128, 128, L)) < 1e-9
+    assert 127.5 < mla.prefill_crossover(prob, 512) < 128.5
+    assert mla.prefill_crossover(prob, 0) == 0.0
