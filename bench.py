@@ -14,6 +14,7 @@ sample of the same workload (the slow baseline arm)."""
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -408,9 +409,12 @@ def main_op(args):
     """One JSON line for a non-headline row of the path, same contract as the decode line."""
     rank, world, local = dist_env()
     active = init_dist(world, args.backend)
-    cfg = CONFIGS["sparse" if args.op == "sparse" and args.config == DEFAULT_CONFIG else args.config]
+    default = {"sparse": "sparse", "prefill": "prefill"}.get(args.op, DEFAULT_CONFIG)
+    cfg = CONFIGS[default if args.config == DEFAULT_CONFIG else args.config]
     if args.op == "sparse":
         return main_sparse(args, cfg, rank, world, local, active)
+    if args.op == "prefill":
+        return main_prefill(args, cfg, rank, world, local, active)
     from mla_decode_attention_absorbed_gb300 import mla
     from mla_decode_attention_absorbed_gb300.workloads import make_append_inputs
 
@@ -538,6 +542,141 @@ def main_op(args):
                 "h2d_bytes_per_step": (h_x.numel() + h_kr.numel()) * 2, "d2h_bytes_per_step": h_rows.numel() * h_rows.element_size(),
                 "note": "pinned host x / k_rope in, the appended cache rows back, every step"},
         "gpu_launches": 2 * args.steps,  # split-K GEMM + scatter (the accumulator memset is a driver op)
+        "clocks": clocks.summary(),
+        "step_ms_min": min(step_ms),
+        "step_ms_median": statistics.median(step_ms),
+    }
+    print(json.dumps(line))
+
+
+def prefill_flops(cfg, lens):
+    """Algorithmic FLOPs of one prefill step in the expand form ("Why MLA and MTP
+    Fight Each Other", 5.3/5.5): K_h, V_h for every cached token of every head,
+    then causal attention over the visible pairs with a (d_nope + d_rope)-wide
+    score and a d_v-wide sum; and in the absorbed form (5.3 / the decode counters)."""
+    from oracle import counts
+    toks = sum(int(L) for L in lens)
+    pairs = sum(counts.visible_pairs(int(L), cfg.s_q) for L in lens)
+    expand = (2 * toks * cfg.H * cfg.d_c * (cfg.d_nope + cfg.d_v)
+              + 2 * pairs * cfg.H * (cfg.d_nope + cfg.d_rope + cfg.d_v))
+    absorbed = (counts.attention_flops(cfg.H, cfg.d_c, cfg.d_rope, lens, cfg.s_q)
+                + counts.absorb_flops(cfg.B, cfg.s_q, cfg.H, cfg.d_nope, cfg.d_c)
+                + counts.out_proj_flops(cfg.B, cfg.s_q, cfg.H, cfg.d_c, cfg.d_v))
+    return expand, absorbed
+
+
+def main_prefill(args, cfg, rank, world, local, active):
+    """Prefill through mla_prefill (expand form above the crossover); the
+    absorbed form is timed beside it where its row limit allows."""
+    from mla_decode_attention_absorbed_gb300 import mla
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    mla.load()
+    c = cfg.with_(seed=replica_seed(cfg.seed, rank))
+    inp = make_inputs(c)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    prob = mla.Problem.of(c)
+    lens = inp["seq_lens"].tolist()
+    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size, max_seq_len=max(lens))
+    f_exp, f_abs = prefill_flops(c, lens)
+    out = torch.empty(c.B, c.s_q, c.H, c.d_v, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(c.B, c.s_q, c.H, dtype=torch.float32, device=dev)
+    ws = mla.alloc_workspace(mla.load().mla_prefill_workspace_size(ctypes.byref(prob.dims()), ctypes.byref(cache)), dev)
+    path = [None]
+
+    def step():
+        path[0] = mla.prefill(prob, d["q_nope"], d["q_rope"], cache, d["w_uk"], d["w_uv"], out=out, lse=lse,
+                              workspace=ws)[3]
+
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    st = mla.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
+    clocks = ClockSampler(local).start()
+    time.sleep(0.3)
+    barrier(active)
+    step_ms = _timed_steps(step, args.steps, flush, stream, dev)
+    barrier(active)
+    clocks.stop()
+    ms = reduce_max(sum(step_ms) / len(step_ms), active, "cuda" if active and args.backend == "nccl" else "cpu")
+    flops = f_exp if path[0] == mla.PATH_EXPAND else f_abs
+    # the absorbed form on the same step, where the absorbed kernels' row limit allows
+    absorbed_ms = None
+    if c.s_q * c.H <= 65536:
+        dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], c.page_size,
+                          max_seq_len=max(lens))
+        for _ in range(args.warmup):
+            flush.zero_()
+            dec(d["q_nope"], d["q_rope"])
+        absorbed_ms = sum(_timed_steps(lambda: dec(d["q_nope"], d["q_rope"]), args.steps, flush, stream, dev)) / args.steps
+    # end to end: pinned q_nope / q_rope in, out back, every step
+    h_qn, h_qr = inp["q_nope"].pin_memory(), inp["q_rope"].pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        d["q_nope"].copy_(h_qn, non_blocking=True)
+        d["q_rope"].copy_(h_qr, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active, "cuda" if active and args.backend == "nccl" else "cpu")
+    if rank != 0:
+        return
+    pk = peaks()
+    ach = flops / (ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        rows = list(range(0, c.B * c.s_q * c.H, max(1, c.B * c.s_q * c.H // 32)))[:32]
+        t = time.perf_counter()
+        oracle.naive(c, inp["q_nope"], inp["q_rope"], inp["kv"], inp["seq_lens"], inp["w_uk"], inp["w_uv"],
+                     inp["block_table"], c.page_size, rows=rows)
+        t = time.perf_counter() - t
+        rows_total = c.B * c.s_q * c.H
+        cpu = {"value": flops * len(rows) / rows_total / t / 1e12, "unit": "TFLOP/s", "cores": oracle.threads(),
+               "kind": "oracle",
+               "sample": f"{len(rows)} of {rows_total} query rows, decompress-then-attend in fp64, {t:.1f} s "
+                         "(the oracle re-expands each row's history: far more work than the sampled share)"}
+    line = {
+        "metric": "MLA prefill TFLOP/s (expand form above the crossover S*, H=128, d_c=512+64, 1xGB300)",
+        "value": flops * world / (ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights)",
+        "config": {"workload": workload_name(c), "path": "expand" if path[0] == mla.PATH_EXPAND else "absorbed",
+                   "crossover_S": mla.prefill_crossover(prob, max(lens)),
+                   "l2": "L2 flushed between steps (256 MB write)",
+                   "parallelism": f"{world} independent replica(s)"},
+        "flops_expand_form": f_exp,
+        "flops_absorbed_form": f_abs,
+        "absorbed_form_ms": absorbed_ms,
+        "roofline": {"bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": ach / pk["bf16_tflops"], "traffic": None,
+                     "kernel": "mla_prefill (expand GEMM + per-head attention) as one step",
+                     "peak_source": pk["source"] + " burst bf16",
+                     "roofline_time_us": flops / (pk["bf16_tflops"] * 1e12) * 1e6, "kernel_us": ms * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": (h_qn.numel() + h_qr.numel()) * 2, "d2h_bytes_per_step": h_out.numel() * 2,
+                "note": "pinned host q_nope/q_rope in, out back, every step; cache and weights resident"},
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
         "step_ms_min": min(step_ms),
         "step_ms_median": statistics.median(step_ms),
@@ -787,7 +926,7 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="latent cache format of the decode and sparse ops (fp8: E4M3 codes, scale 1/16)")
-    ap.add_argument("--op", default="decode", choices=["decode", "append", "sparse"],
+    ap.add_argument("--op", default="decode", choices=["decode", "append", "sparse", "prefill"],
                     help="decode: the absorbed decode step (headline); append: the cache append "
                          "(latent down-projection of the new tokens, d_model = 7168); sparse: the decode "
                          "step with sparse top-k attention (k = 2048, workload 'sparse' by default)")

@@ -71,6 +71,10 @@ CONFIGS = {
     "spec": MLAConfig("spec", B=64, s_q=4, T=8192, **_DSV3),
     # sparse top-k decode: long histories, k = 2048 listed tokens per query token
     "sparse": MLAConfig("sparse", B=64, s_q=1, T=32768, **_DSV3),
+    # prefill: one 4096-token prompt (every token new), and a 512-token chunk after
+    # 3584 cached tokens (above the crossover S* ~ 142 at L = 4096)
+    "prefill": MLAConfig("prefill", B=1, s_q=4096, T=4096, **_DSV3),
+    "chunk": MLAConfig("chunk", B=1, s_q=512, T=4096, **_DSV3),
     # ragged lengths over a shuffled paged pool
     "ragged_paged": MLAConfig("ragged_paged", B=128, s_q=2, len_lo=512, len_hi=16384, paged=True,
                               page_size=64, **_DSV3),
