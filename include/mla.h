@@ -12,6 +12,7 @@
  *                    over a contiguous or paged latent cache, split along the
  *                    history and merged with a log-sum-exp combine
  *   mla_out_proj     out = o_lat . W_UV                               per head
+ *   mla_decode_step  the three above as one call, the kernels overlapping
  *   mla_decode_attn_sparse  the same attention over k listed cached tokens
  *                    per query token (sparse top-k decode)
  *   mla_cache_append c_kv = x . W_DKV of the new tokens, written with their
@@ -267,6 +268,19 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
 MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
                                     void *o_lat, float *lse, int num_splits, int *device_status,
                                     void *stream);
+
+/* One whole absorbed decode step: mla_absorb_q -> mla_decode_attn ->
+ * mla_out_proj with one call, the same arguments and results (q_cat and o_lat
+ * are the caller's intermediate buffers, the workspace is sized by
+ * mla_decode_workspace_size).  The status word is reset first, then the three
+ * kernels are launched back to back; the attention and out_proj grids are
+ * launched programmatically (CUDA programmatic dependent launch), so each starts
+ * while its predecessor runs -- the attention streaming its first cache tiles,
+ * out_proj its W_UV tiles -- and reads the predecessor's output only once that
+ * grid has completed. */
+MLA_API int mla_decode_step(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+                            const void *w_uk, const void *w_uv, void *q_cat, void *o_lat, void *out, float *lse,
+                            void *workspace, size_t ws_bytes, int num_splits, void *stream);
 
 /* Which path mla_prefill took. */
 typedef enum { MLA_PATH_ABSORB = 0, MLA_PATH_EXPAND = 1 } mla_path;

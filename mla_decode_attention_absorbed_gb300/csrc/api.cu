@@ -459,6 +459,51 @@ MLA_API int mla_prefill(const mla_dims *dims, const void *q_nope, const void *q_
     return mla_out_proj(dims, o_lat, w_uv, out, stream);
 }
 
+MLA_API int mla_decode_step(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+                            const void *w_uk, const void *w_uv, void *q_cat, void *o_lat, void *out, float *lse,
+                            void *workspace, size_t ws_bytes, int num_splits, void *stream) {
+    int s = check_dims(dims);
+    if (s) return s;
+    if (!cache) return MLA_ERR_NULL;
+    if ((s = check_cache(dims, cache))) return s;
+    if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (!workspace) return MLA_ERR_NULL;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    const int splits = plan_splits(dims, cache, num_splits);
+    if (ws_bytes < attn_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    if (dims->B > 0) {
+        if (!q_nope || !w_uk || !w_uv || !q_cat || !o_lat || !out || !lse || (dims->d_rope && !q_rope))
+            return MLA_ERR_NULL;
+        if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(q_cat) || !aligned16(o_lat) ||
+            !aligned16(out) || !aligned16(lse) || (q_rope && !aligned16(q_rope)))
+            return MLA_ERR_ALIGN;
+    }
+    cudaStream_t st = as_stream(stream);
+    // the status reset comes first, so that nothing but kernels separates the three
+    // launches: the attention and out_proj grids are launched programmatically and
+    // start while their predecessor runs, reading its output only once it completed
+    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (dims->B == 0) return MLA_OK;
+    cudaError_t e = mla::launch_absorb_q_tc(*dims, q_nope, q_rope, w_uk, q_cat, st, true);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    mla::AttnParams p = make_params(dims, cache);
+    p.q_cat = (const __nv_bfloat16 *)q_cat;
+    p.o_lat = (__nv_bfloat16 *)o_lat;
+    p.lse = lse;
+    p.num_splits = splits;
+    p.status = (int *)workspace;
+    p.pdl = 1;
+    if (splits > 1) {
+        size_t rows = (size_t)dims->B * splits * dims->s_q * dims->H;
+        char *base = (char *)workspace + kStatusBytes;
+        p.part_ml = (float *)base;
+        p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
+    }
+    if ((e = mla::launch_attn_tc(p, st)) != cudaSuccess) return MLA_ERR_CUDA;
+    e = mla::launch_out_proj_tc(*dims, o_lat, w_uv, out, st, true);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 MLA_API int mla_read_status(const void *workspace, int *status, void *stream) {
     if (!workspace || !status) return MLA_ERR_NULL;
     int v = 0;

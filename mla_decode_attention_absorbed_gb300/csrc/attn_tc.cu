@@ -287,6 +287,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (p.pdl) pdl_launch_dependents();
     const uint32_t rank = kSplit ? cluster_rank() : 0;
     const uint32_t peer = rank ^ 1u;
     const Geo g = rank == 0 ? g0 : g1;
@@ -712,6 +713,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         // log2 units directly; the two warps of a quadrant take alternate
         // 32-channel chunks; padding rows and channels are zero
         {
+            if (p.pdl) pdl_wait();  // q_cat comes from the grid this one overlaps
             const int QW = p.q_w > 0 ? p.q_w : W;
             const __nv_bfloat16 *qrow = p.q_cat + row_index(gr) * QW;
             for (int c0 = 32 * hf; c0 < g.sw; c0 += 64) {
@@ -1028,13 +1030,15 @@ cudaError_t launch_variant(const CUtensorMap &tm0, const CUtensorMap &tm1, const
     cfg.blockDim = dim3(threads_of(kSparse, kFp8));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kSplit ? 2 : 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = p.pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, tm0, tm1, p, g0, g1);
 }
 

@@ -35,6 +35,10 @@ struct AttnParams {
     // query / output / lse rows are [seq][s_q][heads_per_seq] (0 or 1: plain)
     int heads_per_seq;
     int q_w;                      // elements per q_cat row (0: d_c + d_rope)
+    // launched programmatically right after the grid that writes q_cat (a fused
+    // decode step): q_cat is read only once that grid has completed, and the next
+    // grid (out_proj) may start its CTAs at once
+    int pdl;
 };
 
 // Record the first device-side error; later ones keep the first.

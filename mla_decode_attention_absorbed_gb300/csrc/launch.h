@@ -7,9 +7,13 @@
 
 namespace mla {
 
+// trigger: let the next grid (launched programmatically) start its CTAs at once;
+// wait_prev: this grid is launched programmatically after the attention and
+// reads o_lat only once that grid has completed.
 cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void *q_rope, const void *w_uk,
-                               void *q_cat, cudaStream_t st);
-cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void *w_uv, void *out, cudaStream_t st);
+                               void *q_cat, cudaStream_t st, bool trigger = false);
+cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void *w_uv, void *out, cudaStream_t st,
+                               bool wait_prev = false);
 // Split-K plan of the cache append's down-projection: 64-column N tiles, and
 // K (d_model, in 64-wide chunks) cut so that all tiles together make about one
 // CTA per SM.  Partials: splits * M * d_c fp32.

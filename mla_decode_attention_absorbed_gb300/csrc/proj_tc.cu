@@ -39,15 +39,25 @@ struct ProjArgs {
     float *acc;            // split K: fp32 partials [splits][M][N] instead of `out`
     int kc_per_cta;        // split K: 64-wide K chunks per CTA
     int splits;            // split K: CTAs along K (grid z)
+    // programmatic dependent launch inside a fused decode step: this grid may start
+    // while the previous one runs and reads A (its output) only after it completed;
+    // and / or lets the next grid start its CTAs right away
+    bool wait_a;
+    bool trigger;
 };
 
+// BN = 512 (absorb at d_c = 512: a whole head per CTA, one wave of CTAs) runs two
+// N = 256 MMAs per K step into the two halves of tensor memory, with a 2-stage
+// ring (K = d_nope is two chunks).
 template <int BN>
 struct ProjSmem {
-    static constexpr uint32_t kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+    static constexpr uint32_t kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : BN <= 256 ? 256 : 512;
+    static constexpr int kStagesN = BN > 256 ? 2 : kStages;
+    static constexpr int kHalves = BN > 256 ? 2 : 1;   // MMAs of N = BN / kHalves per K step
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
     static constexpr int kBBytes = BN * kBK * 2;   // 32 KB at BN = 256
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kBytes = kStages * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+    static constexpr int kBytes = kStagesN * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
 };
 
 template <int BN, bool kBMN>
@@ -57,9 +67,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment: the 128-byte swizzle pattern repeats every 8 rows of 128 B
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using L = ProjSmem<BN>;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * L::kStageBytes);
-    uint64_t *empty = full + kStages;
-    uint64_t *acc_full = empty + kStages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kStagesN * L::kStageBytes);
+    uint64_t *empty = full + L::kStagesN;
+    uint64_t *acc_full = empty + L::kStagesN;
     uint32_t *tmem_base_slot = reinterpret_cast<uint32_t *>(acc_full + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_base_slot + 1);
 
@@ -69,9 +79,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = g.acc ? 0 : blockIdx.z;
     const int kc0 = g.acc ? blockIdx.z * g.kc_per_cta : 0;
     const int nk = g.acc ? min(g.kc_per_cta, nk_all - kc0) : nk_all;
+    if (g.trigger) pdl_launch_dependents();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < L::kStagesN; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -89,31 +100,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 && lane == 0) {
         // ---------------- TMA producer
+        // After a programmatic launch the weight chunks of the first stages are
+        // fetched while the previous grid still runs; A, its output, only once it
+        // has completed.
+        const int early = g.wait_a ? min(nk, L::kStagesN) : 0;
+        auto load_b = [&](int kc) {
+            const int s = kc % L::kStagesN;
+            uint8_t *sb = smem + s * L::kStageBytes + L::kABytes;
+            const int kx = (kc0 + kc) * kBK;
+            if (kBMN) {
+                for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tmB, &full[s], n0 + 64 * j, kx, h);
+            } else {
+                for (int j = 0; j < L::kHalves; ++j)
+                    tma_load_3d(sb + j * (BN / L::kHalves) * 128, &tmB, &full[s], kx, n0 + j * (BN / L::kHalves), h);
+            }
+        };
+        for (int kc = 0; kc < early; ++kc) {
+            mbar_arrive_expect_tx(&full[kc], L::kStageBytes);
+            load_b(kc);
+        }
+        if (g.wait_a) pdl_wait();
         for (int kc = 0; kc < nk; ++kc) {
-            const int s = kc % kStages;
-            if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1)) {
+            const int s = kc % L::kStagesN;
+            if (kc >= L::kStagesN && !mbar_wait(&empty[s], ((kc / L::kStagesN) - 1) & 1)) {
                 *abort_flag = 1;
                 break;
             }
             if (*abort_flag) break;
             uint8_t *sa = smem + s * L::kStageBytes;
-            uint8_t *sb = sa + L::kABytes;
             const int kx = (kc0 + kc) * kBK;
-            mbar_arrive_expect_tx(&full[s], L::kStageBytes);
+            if (kc >= early) mbar_arrive_expect_tx(&full[s], L::kStageBytes);
             tma_load_3d(sa, &tmA, &full[s], kx, h, m0);
-            if (kBMN) {
-                for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * 64 * 128, &tmB, &full[s], n0 + 64 * j, kx, h);
-            } else {
-                tma_load_3d(sb, &tmB, &full[s], kx, n0, h);
-            }
+            if (kc >= early) load_b(kc);
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------- MMA issuer
-        constexpr uint32_t idesc = idesc_bf16(kBM, BN, false, kBMN);
+        constexpr uint32_t idesc = idesc_bf16(kBM, BN / L::kHalves, false, kBMN);
         bool ok = true;
         for (int kc = 0; kc < nk && ok; ++kc) {
-            const int s = kc % kStages;
-            if (!mbar_wait(&full[s], (kc / kStages) & 1)) {
+            const int s = kc % L::kStagesN;
+            if (!mbar_wait(&full[s], (kc / L::kStagesN) & 1)) {
                 *abort_flag = 1;
                 ok = false;
                 break;
@@ -124,9 +150,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
                 const uint64_t da = smem_desc_sw128(sa + kk * 32, 16, 1024);
-                const uint64_t db = kBMN ? smem_desc_sw128(sb + kk * 16 * 128, 64 * 128, 1024)
-                                         : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                mma_ss(tmem, da, db, idesc, (kc | kk) != 0);
+#pragma unroll
+                for (int j = 0; j < L::kHalves; ++j) {
+                    const uint64_t db = kBMN ? smem_desc_sw128(sb + kk * 16 * 128, 64 * 128, 1024)
+                                             : smem_desc_sw128(sb + j * (BN / L::kHalves) * 128 + kk * 32, 16, 1024);
+                    mma_ss(tmem + j * (BN / L::kHalves), da, db, idesc, (kc | kk) != 0);
+                }
             }
             mma_commit(&empty[s]);  // the stage is free once these MMAs have read it
         }
@@ -136,10 +165,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = q * 32 + lane;
         const int m = m0 + row;
-        const bool ok = (nk <= 0 || mbar_wait(acc_full, 0)) && !*abort_flag;
+        // a quadrant without a valid row (fewer than 128 tokens) has nothing to store
+        const bool live = m0 + q * 32 < g.M;
+        const bool ok = live && (nk <= 0 || mbar_wait(acc_full, 0)) && !*abort_flag;
         tc_fence_after();
         const int n_valid = g.N - n0;  // a multiple of 16
-        if (g.acc) {
+        if (g.acc && live) {
             // split K: this CTA's fp32 tile is split blockIdx.z's partial (zeros if it has no K)
             float *prow = g.acc + ((long long)blockIdx.z * g.M + m) * g.N + n0;
             for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -158,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __nv_bfloat16 *dst = g.acc ? nullptr : g.out + ((long long)m * g.H + h) * g.out_row + n0;
-        for (int c0 = 0; !g.acc && c0 < BN; c0 += 16) {
+        for (int c0 = 0; live && !g.acc && c0 < BN; c0 += 16) {
             uint32_t r[16];
             tmem_ld16(tmem + tmem_lane_base(q) + c0, r);
             tmem_ld_wait();
@@ -194,9 +225,17 @@ cudaError_t launch_proj(const CUtensorMap &tA, const CUtensorMap &tB, const Proj
     const int smem = ProjSmem<BN>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<BN, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((g.N + BN - 1) / BN, (g.M + kBM - 1) / kBM, g.acc ? g.splits : g.H);
-    proj_gemm_tc<BN, kBMN><<<grid, kThreads, smem, st>>>(tA, tB, g);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((g.N + BN - 1) / BN, (g.M + kBM - 1) / kBM, g.acc ? g.splits : g.H);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g.wait_a ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, proj_gemm_tc<BN, kBMN>, tA, tB, g);
 }
 
 // A operand [M][H][K] bf16 (K contiguous), box 64 x 1 x 128.
@@ -211,19 +250,20 @@ bool map_rows(CUtensorMap *m, const void *base, int M, int H, int K) {
 
 // q_cat = [q_nope . W_UK^T | q_rope]
 cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void *q_rope, const void *w_uk,
-                               void *q_cat, cudaStream_t st) {
+                               void *q_cat, cudaStream_t st, bool trigger) {
     const int M = d.B * d.s_q;
     CUtensorMap tA, tB;
     if (!map_rows(&tA, q_nope, M, d.H, d.d_nope)) return cudaErrorInvalidValue;
     // W_UK [H][d_c][d_nope]: K-major B, box 64 (k) x BN (n) x 1
-    const int BN = d.d_c >= 256 ? 256 : d.d_c;  // d_c is a multiple of 64
+    const int BN = d.d_c == 512 ? 512 : d.d_c >= 256 ? 256 : d.d_c;  // d_c is a multiple of 64
     uint64_t dims[3] = {(uint64_t)d.d_nope, (uint64_t)d.d_c, (uint64_t)d.H};
     uint64_t strides[2] = {(uint64_t)d.d_nope * 2, (uint64_t)d.d_c * d.d_nope * 2};
-    uint32_t box[3] = {64, (uint32_t)BN, 1};
+    uint32_t box[3] = {64, (uint32_t)(BN > 256 ? 256 : BN), 1};
     if (!encode_bf16_sw128(&tB, w_uk, 3, dims, strides, box)) return cudaErrorInvalidValue;
     ProjArgs g{M, d.H, d.d_c, d.d_nope, (__nv_bfloat16 *)q_cat, d.d_c + d.d_rope,
-               d.d_rope ? (const __nv_bfloat16 *)q_rope : nullptr, d.d_rope, nullptr, 0, 1};
+               d.d_rope ? (const __nv_bfloat16 *)q_rope : nullptr, d.d_rope, nullptr, 0, 1, false, trigger};
     switch (BN) {
+        case 512: return launch_proj<512, false>(tA, tB, g, st);
         case 256: return launch_proj<256, false>(tA, tB, g, st);
         case 192: return launch_proj<192, false>(tA, tB, g, st);
         case 128: return launch_proj<128, false>(tA, tB, g, st);
@@ -233,7 +273,8 @@ cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void
 }
 
 // out = o_lat . W_UV
-cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void *w_uv, void *out, cudaStream_t st) {
+cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void *w_uv, void *out, cudaStream_t st,
+                               bool wait_prev) {
     const int M = d.B * d.s_q;
     CUtensorMap tA, tB;
     if (!map_rows(&tA, o_lat, M, d.H, d.d_c)) return cudaErrorInvalidValue;
@@ -242,7 +283,7 @@ cudaError_t launch_out_proj_tc(const mla_dims &d, const void *o_lat, const void 
     uint64_t strides[2] = {(uint64_t)d.d_v * 2, (uint64_t)d.d_c * d.d_v * 2};
     uint32_t box[3] = {64, 64, 1};
     if (!encode_bf16_sw128(&tB, w_uv, 3, dims, strides, box)) return cudaErrorInvalidValue;
-    ProjArgs g{M, d.H, d.d_v, d.d_c, (__nv_bfloat16 *)out, d.d_v, nullptr, 0, nullptr, 0, 1};
+    ProjArgs g{M, d.H, d.d_v, d.d_c, (__nv_bfloat16 *)out, d.d_v, nullptr, 0, nullptr, 0, 1, wait_prev, false};
     switch ((d.d_v + 63) / 64 * 64) {  // MMA width: d_v rounded up to whole 64-column boxes
         case 256: return launch_proj<256, true>(tA, tB, g, st);
         case 192: return launch_proj<192, true>(tA, tB, g, st);
@@ -356,7 +397,7 @@ cudaError_t launch_cache_append_tc(const AttnParams &p, int d_model, const void 
     uint32_t box[3] = {64, 64, 1};
     if (!encode_bf16_sw128(&tB, w_dkv, 3, dims, strides, box)) return cudaErrorInvalidValue;
     const AppendPlan plan = append_plan(M, p.d_c, d_model);
-    ProjArgs g{M, 1, p.d_c, d_model, nullptr, 0, nullptr, 0, part, plan.kc_per_cta, plan.splits};
+    ProjArgs g{M, 1, p.d_c, d_model, nullptr, 0, nullptr, 0, part, plan.kc_per_cta, plan.splits, false, false};
     cudaError_t e = launch_proj<64, true>(tA, tB, g, st);
     if (e != cudaSuccess) return e;
     append_scatter<<<M, kScatterThreads, 0, st>>>(p, part, plan.splits, (const __nv_bfloat16 *)k_rope);

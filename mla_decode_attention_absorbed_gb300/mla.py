@@ -44,7 +44,8 @@ EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_w
            "mla_decode_num_splits", "mla_decode_attn", "mla_out_proj", "mla_naive_workspace_size",
            "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc", "mla_cache_append_workspace_size",
            "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse", "mla_prefill_crossover",
-           "mla_prefill_expand_workspace_size", "mla_prefill_expand", "mla_prefill_workspace_size", "mla_prefill")
+           "mla_prefill_expand_workspace_size", "mla_prefill_expand", "mla_prefill_workspace_size", "mla_prefill",
+           "mla_decode_step")
 PATH_ABSORB, PATH_EXPAND = 0, 1
 
 
@@ -90,6 +91,8 @@ def load(path: str | None = None):
     lib.mla_cache_append.restype = I
     lib.mla_read_status.argtypes = [P, ctypes.POINTER(I), P]
     lib.mla_read_status.restype = I
+    lib.mla_decode_step.argtypes = [pd, P, P, pc, P, P, P, P, P, P, P, SZ, I, P]
+    lib.mla_decode_step.restype = I
     lib.mla_prefill_crossover.argtypes = [pd, ctypes.c_longlong]
     lib.mla_prefill_crossover.restype = ctypes.c_double
     lib.mla_prefill_expand_workspace_size.argtypes = [pd, pc]
@@ -394,6 +397,15 @@ class Decoder:
 
     def project(self, stream=None):
         return out_proj(self.prob, self.o_lat, self.w_uv, self.out, stream)
+
+    def step(self, q_nope, q_rope, stream=None):
+        """mla_decode_step: the three launches as one call, overlapping."""
+        d = self.prob.dims()
+        _check(load().mla_decode_step(ctypes.byref(d), _ptr(q_nope), _ptr(q_rope), ctypes.byref(self.cache),
+                                      _ptr(self.w_uk), _ptr(self.w_uv), _ptr(self.q_cat), _ptr(self.o_lat),
+                                      _ptr(self.out), _ptr(self.lse), _ptr(self.workspace), self.workspace.numel(),
+                                      int(self.num_splits), _stream(stream)), "mla_decode_step")
+        return self.out
 
     def __call__(self, q_nope, q_rope, stream=None):
         self.absorb(q_nope, q_rope, stream)

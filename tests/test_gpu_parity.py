@@ -171,3 +171,26 @@ def test_naive_path_matches_oracle(cfg):
     # and the absorbed GPU path agrees with it
     g = run_gpu(cfg, inp)
     within_tolerance(g["out"], ref_out, "absorbed vs naive reference")
+
+
+@pytest.mark.parametrize("name,splits", [("dsv3", 0), ("long", 0), ("spec", 0)])
+def test_fused_step_matches_separate_calls(name, splits):
+    """mla_decode_step (programmatically overlapped launches) gives bit for bit the
+    results of the three separate calls, and matches the oracle on sampled rows."""
+    from helpers import sample_rows
+    cfg = CONFIGS[name].with_(B=min(CONFIGS[name].B, 16))
+    inp = make_inputs(cfg)
+    d = to_dev(inp)
+    prob = mla.Problem.of(cfg)
+    dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], cfg.page_size,
+                      num_splits=splits)
+    for _ in range(2):
+        out_f = dec.step(d["q_nope"], d["q_rope"]).clone()
+    lse_f = dec.lse.clone()
+    assert mla.read_status(dec.workspace) == 0
+    out_s = dec(d["q_nope"], d["q_rope"]).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out_f, out_s) and torch.equal(lse_f, dec.lse)
+    rows = sample_rows(cfg, 24)
+    g = dict(q_cat=dec.q_cat.cpu(), o_lat=dec.o_lat.cpu(), lse=lse_f.cpu(), out=out_f.cpu())
+    check_against_oracle(cfg, inp, g, rows=rows)
