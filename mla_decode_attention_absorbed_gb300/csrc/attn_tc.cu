@@ -266,6 +266,38 @@ __device__ __forceinline__ void convert_fp8_tile(uint8_t *dst, const uint8_t *sr
     }
 }
 
+// Dense FP8 tiles arrive box by box: the 64 codes of each row of box b (64
+// channels) land, 64 rows x 64 B, in the upper half of the box's own 8 KB output
+// region.  convert_fp8_rows turns rows [r0, r0 + 16 * kRowGroups) of such a raw
+// box into the swizzled fp16 box: raw chunk c (16 codes) of row r becomes output
+// chunks 2c and 2c + 1 of row r, at chunks (2c) ^ (r % 8) and (2c + 1) ^ (r % 8).
+// Lane l takes raw chunk l % 4 of row r0 + l / 4 (+ 8 per step): two
+// neighbouring rows land in disjoint bank groups, so the stores do not conflict.
+// All loads come first; `all_read()` then returns whether to store (the raw box
+// lies inside the output box).  Rows whose bit in vmask is clear become zeros.
+template <int kRowGroups, class AllRead>
+__device__ __forceinline__ void convert_fp8_rows(uint8_t *box, int r0, unsigned long long vmask, int lane,
+                                                 AllRead &&all_read) {
+    constexpr int kSteps = kRowGroups * 2;  // 8 rows per step
+    const uint8_t *raw = box + 4096;
+    uint4 in[kSteps];
+#pragma unroll
+    for (int i = 0; i < kSteps; ++i) {
+        const int r = r0 + 8 * i + (lane >> 2), c = lane & 3;
+        in[i] = ((vmask >> r) & 1ull) ? *reinterpret_cast<const uint4 *>(raw + r * 64 + c * 16) : make_uint4(0, 0, 0, 0);
+    }
+    if (!all_read()) return;
+#pragma unroll
+    for (int i = 0; i < kSteps; ++i) {
+        const int r = r0 + 8 * i + (lane >> 2), c = lane & 3, sw = r & 7;
+        const uint2 a = e4m3x4_to_f16x4(in[i].x), b = e4m3x4_to_f16x4(in[i].y);
+        const uint2 d = e4m3x4_to_f16x4(in[i].z), e = e4m3x4_to_f16x4(in[i].w);
+        uint8_t *row = box + r * 128;
+        *reinterpret_cast<uint4 *>(row + (((2 * c) ^ sw) << 4)) = make_uint4(a.x, a.y, b.x, b.y);
+        *reinterpret_cast<uint4 *>(row + (((2 * c + 1) ^ sw) << 4)) = make_uint4(d.x, d.y, e.x, e.y);
+    }
+}
+
 // Instruction descriptor of the kernel's MMAs: bf16 operands, or fp16 for an FP8 cache.
 template <bool kFp8>
 __device__ __forceinline__ uint32_t idesc_of(int M, int N, bool a_mn, bool b_mn) {
@@ -472,10 +504,13 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         // (which may hold anything) and a bad page's rows are zeroed by the converters
                         const int cnt = page_ok ? min(kTile, L - (t0 + n * kTile)) : 0;
                         sm.valid[s] = cnt >= kTile ? ~0ull : ((1ull << cnt) - 1ull);
-                        mbar_arrive_expect_tx(&sm.landed[s], kTile * g.pitch);
-                        uint8_t *raw = sm.kv[s] + kStageBytes - kTile * g.pitch;
-                        if (kPaged) tma_load_2d(raw, tm, &sm.landed[s], g.x_u32, y);
-                        else tma_load_3d(raw, tm, &sm.landed[s], g.x_u32, y, z);
+                        // box by box: 64 rows x 64 codes into the upper half of each output box
+                        mbar_arrive_expect_tx(&sm.landed[s], g.nbox * 4096);
+                        for (int bx = 0; bx < g.nbox; ++bx) {
+                            uint8_t *raw = sm.kv[s] + bx * kBoxBytes + 4096;
+                            if (kPaged) tma_load_2d(raw, tm, &sm.landed[s], g.x_u32 + 16 * bx, y);
+                            else tma_load_3d(raw, tm, &sm.landed[s], g.x_u32 + 16 * bx, y, z);
+                        }
                     } else {
                         mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
                         for (int bx = 0; bx < g.nbox; ++bx) {
@@ -677,13 +712,27 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                     break;
                 }
                 bool ok = true;
-                convert_fp8_tile<kNConv>(sm.kv[s], sm.kv[s] + kStageBytes - kTile * g.pitch, g.pitch, ncin,
-                                         sm.valid[s], cw, lane, [&]() {
-                                             __syncwarp();
-                                             if (lane == 0) mbar_arrive(&sm.read[s]);  // release: the loads are done
-                                             ok = warp_wait(sm, &sm.read[s], par);
-                                             return ok;
-                                         });
+                auto all_read = [&]() {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.read[s]);  // release: the loads are done
+                    ok = warp_wait(sm, &sm.read[s], par);
+                    return ok;
+                };
+                if constexpr (kSparse) {
+                    // whole row slices: every converter's codes may lie under any output
+                    convert_fp8_tile<kNConv>(sm.kv[s], sm.kv[s] + kStageBytes - kTile * g.pitch, g.pitch, ncin,
+                                             sm.valid[s], cw, lane, all_read);
+                } else {
+                    // box cw (if any) alone, in place; a fifth box (the RoPE key's) shared by all
+                    // four, 16 rows each, behind the read barrier
+                    const unsigned long long vm = sm.valid[s];
+                    if (cw < g.nbox && cw < 4)  // the warp's own loads precede its stores
+                        convert_fp8_rows<4>(sm.kv[s] + cw * kBoxBytes, 0, vm, lane, [] {
+                            __syncwarp();
+                            return true;
+                        });
+                    if (g.nbox > 4) convert_fp8_rows<1>(sm.kv[s] + 4 * kBoxBytes, 16 * cw, vm, lane, all_read);
+                }
                 if (!ok) {
                     if (lane == 0) raise_abort<kSplit>(sm, p, peer);
                     break;
@@ -1075,15 +1124,16 @@ bool encode_slice_map(CUtensorMap *tm, const AttnParams &p, const Geo &g, bool s
         uint32_t box[2] = {box_x, 1};
         return encode_u32_plain(tm, p.kv, 2, dims, strides, box);
     }
+    // dense: one 64-channel box (64 codes = 16 words) of 64 rows per copy
     if (p.block_table) {
         uint64_t dims[2] = {row_u32, (uint64_t)p.num_pages * p.page_size};
         uint64_t strides[1] = {(uint64_t)W * eb};
-        uint32_t box[2] = {box_x, kTile};
+        uint32_t box[2] = {16, kTile};
         return encode_u32_plain(tm, p.kv, 2, dims, strides, box);
     }
     uint64_t dims[3] = {row_u32, (uint64_t)p.capacity, (uint64_t)p.B};
     uint64_t strides[2] = {(uint64_t)W * eb, (uint64_t)p.seq_stride * eb};
-    uint32_t box[3] = {box_x, kTile, 1};
+    uint32_t box[3] = {16, kTile, 1};
     return encode_u32_plain(tm, p.kv, 3, dims, strides, box);
 }
 
