@@ -750,6 +750,8 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         const int gr = rb * kRows + r;
         const bool row_ok = seq_ok && gr < rows_total;
         const int qi = row_ok ? gr / p.H : 0;
+        // the block's earliest query: a tile it sees whole, every row of the block sees whole
+        const int q_first = (rb * kRows) / p.H;
         const int lim = L - p.s_q + qi;  // last visible token of this row
         const uint32_t lane_base = tmem_lane_base(quad);
         // an FP8 cache's scale multiplies every key element: fold it into Q
@@ -872,7 +874,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             // sparse: the producer's per-row flags (listed, visible to this block's query, good page)
             const unsigned long long vmask = kSparse ? sm.valid[n % kRing] : 0ull;
             const bool whole = kSparse ? vmask == ~0ull
-                                       : tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q;
+                                       : tile_ok && tok0 + kTile <= t1 && tok0 + kTile - 1 <= L - p.s_q + q_first;
             float mx0 = -INFINITY, mx1 = -INFINITY;
             if (whole) {
 #pragma unroll
