@@ -337,6 +337,13 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     // [t0, t1): token positions (dense) or positions in the sparse list
     int t0 = 0, t1 = 0;
     if (seq_ok) split_range(kSparse ? p.topk : L, p.num_splits, split, t0, t1);
+    if (!kSparse && seq_ok) {
+        // no row of this block sees a token past its last query's causal limit:
+        // those tiles are not streamed at all (with many new tokens -- a prefill --
+        // this halves the work)
+        const int q_last = min(p.s_q - 1, ((rb + 1) * kRows - 1) / p.H);
+        t1 = max(t0, min(t1, L - p.s_q + q_last + 1));
+    }
     const int ntiles = (t1 - t0 + kTile - 1) / kTile;
 
     if (threadIdx.x == 0) {
