@@ -113,6 +113,7 @@ __device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.a
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
 constexpr uint32_t kBarPairBase = 1;  // named barrier 1 + quadrant: the two warps of a quadrant (64 threads)
+constexpr uint32_t kBarEpilogue = 5;  // all softmax warps: O rows staged in shared memory
 
 struct Geo {
     int k0;      // first channel of this CTA's contraction slice (= first latent column of its O slice)
@@ -496,6 +497,13 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                 int issued = 0;
                 for (int n = 0; n < ntiles; ++n) {
                     const int s = n % kRing;
+                    // Without a preceding grid, every CTA starts at once: the first tile
+                    // goes out, the rest of the ring waits until the queries are in,
+                    // which otherwise queue in HBM behind every CTA's whole ring.
+                    if (n == 1 && !p.pdl && !wait_bar(sm, &sm.q_ready, 0)) {
+                        raise_abort<kSplit>(sm, p, peer);
+                        break;
+                    }
                     if (n >= kRing && !wait_bar(sm, &sm.empty[s], ((n / kRing) - 1) & 1)) {
                         raise_abort<kSplit>(sm, p, peer);
                         break;
@@ -769,27 +777,60 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         // Q slice -> TMEM (bf16 pairs, fp16 with an FP8 cache), pre-multiplied by
         // scale * log2(e) (* kv_scale) so that the score MMAs produce exponents in
         // log2 units directly; the two warps of a quadrant take alternate
-        // 32-channel chunks; padding rows and channels are zero
+        // 32-channel chunks; padding rows and channels are zero.  A warp reads a
+        // chunk of its 32 rows as 8 rows x 64 contiguous bytes per instruction (one
+        // row per lane would touch 32 lines per instruction), every chunk's loads in
+        // flight at once, and turns it into one row per lane through its own 2 KB
+        // of the score staging buffer (idle until the first tile's scores),
+        // 16-byte pieces XOR-swizzled by row so both passes are conflict-free.
         {
             if (p.pdl) pdl_wait();  // q_cat comes from the grid this one overlaps
             const int QW = p.q_w > 0 ? p.q_w : W;
-            const __nv_bfloat16 *qrow = p.q_cat + row_index(gr) * QW;
-            for (int c0 = 32 * hf; c0 < g.sw; c0 += 64) {
+            const int lr = lane >> 2, lj = lane & 3;  // load pass: row (of 8) and 16-byte piece
+            const __nv_bfloat16 *src[4];
+            bool src_ok[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int gq = rb * kRows + quad * 32 + 8 * k + lr;
+                src_ok[k] = seq_ok && gq < rows_total;
+                src[k] = p.q_cat + (src_ok[k] ? row_index(gq) * QW : 0);
+            }
+            uint4 qv[kMaxBoxes][4];
+#pragma unroll
+            for (int i = 0; i < kMaxBoxes; ++i) {
+                const int c = 32 * hf + 64 * i + lj * 8;  // first channel of this lane's piece
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    qv[i][k] = make_uint4(0, 0, 0, 0);
+                    if (src_ok[k] && c < g.sw && g.qk0 + c < QW)
+                        qv[i][k] = *reinterpret_cast<const uint4 *>(src[k] + g.qk0 + c);
+                }
+            }
+            uint8_t *slot = reinterpret_cast<uint8_t *>(sm.tx) + warp * 2048;
+#pragma unroll
+            for (int i = 0; i < kMaxBoxes; ++i) {
+                const int c0 = 32 * hf + 64 * i;
+                if (c0 >= g.sw) break;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int R = 8 * k + lr;
+                    *reinterpret_cast<uint4 *>(slot + R * 64 + ((lj ^ ((R >> 1) & 3)) << 4)) = qv[i][k];
+                }
+                __syncwarp();
                 uint32_t v[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    uint4 u = make_uint4(0, 0, 0, 0);
-                    const int ch = g.qk0 + c0 + e * 8;
-                    if (row_ok && ch < QW && c0 + e * 8 < g.sw) u = *reinterpret_cast<const uint4 *>(qrow + ch);
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(slot + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
                     const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[k]);
+                    for (int e = 0; e < 4; ++e) {
+                        const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&w4[e]);
                         const float2 f = __bfloat1622float2(h);
-                        v[e * 4 + k] = kFp8 ? pack_f16x2(f.x * scale_log2, f.y * scale_log2)
+                        v[j * 4 + e] = kFp8 ? pack_f16x2(f.x * scale_log2, f.y * scale_log2)
                                             : pack_bf16x2(f.x * scale_log2, f.y * scale_log2);
                     }
                 }
+                __syncwarp();
                 tmem_st16(tmem + lane_base + kColQ + c0 / 2, v);
             }
             tmem_st_wait();
@@ -984,9 +1025,15 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         const bool any = have_o && l_row > 0.f;
         // an FP8 cache's scale multiplies every value element
         const float vscale = kFp8 ? p.kv_scale : 1.f;
+        // O leaves through shared memory: each thread writes its row's columns into a
+        // staging copy (the operand ring is idle once the last sum has landed), then
+        // the softmax warps store whole rows, consecutive lanes on consecutive 16-byte
+        // chunks, instead of one 16-byte piece of 32 different rows per instruction.
+        uint8_t *stg = &sm.kv[0][0];
+        const int eb = p.num_splits == 1 ? 2 : 4;  // bf16 output or fp32 partial
+        const int row_bytes = g.vn * eb, pitch = row_bytes + 16;
         if (p.num_splits == 1) {
             const float inv = any ? vscale / l_row : 0.f;
-            __nv_bfloat16 *dst = p.o_lat + row_index(gr) * p.d_c + g.k0;
             for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
                 tmem_ld16(tmem + lane_base + kColO + c, u);
@@ -996,34 +1043,43 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                 for (int e = 0; e < 8; ++e)
                     o8[e] = pack_bf16x2(any ? __uint_as_float(u[2 * e]) * inv : 0.f,
                                         any ? __uint_as_float(u[2 * e + 1]) * inv : 0.f);
-                if (store) {
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
-                    d4[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
-                    d4[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
-                }
+                uint4 *d4 = reinterpret_cast<uint4 *>(stg + r * pitch + c * 2);
+                d4[0] = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+                d4[1] = make_uint4(o8[4], o8[5], o8[6], o8[7]);
             }
             if (store && rank == 0 && hf == 0)
                 p.lse[row_index(gr)] = any ? (m2 + __log2f(l_row)) * ln2 : -INFINITY;
         } else {
             const long long prow = ((long long)b * p.num_splits + split) * rows_total + gr;
-            float *dst = p.part_acc + prow * p.d_c + g.k0;
             for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
                 tmem_ld16(tmem + lane_base + kColO + c, u);
                 tmem_ld_wait();
-                if (store) {
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c);
+                float4 *d4 = reinterpret_cast<float4 *>(stg + r * pitch + c * 4);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        d4[e] = any ? make_float4(__uint_as_float(u[4 * e]) * vscale, __uint_as_float(u[4 * e + 1]) * vscale,
-                                                  __uint_as_float(u[4 * e + 2]) * vscale,
-                                                  __uint_as_float(u[4 * e + 3]) * vscale)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+                for (int e = 0; e < 4; ++e)
+                    d4[e] = any ? make_float4(__uint_as_float(u[4 * e]) * vscale, __uint_as_float(u[4 * e + 1]) * vscale,
+                                              __uint_as_float(u[4 * e + 2]) * vscale,
+                                              __uint_as_float(u[4 * e + 3]) * vscale)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
             }
             if (store && hf == 0) {  // this CTA's (m, l): its half of the columns is relative to them
                 p.part_ml[(prow * 2 + rank) * 2 + 0] = any ? m2 * ln2 : -INFINITY;
                 p.part_ml[(prow * 2 + rank) * 2 + 1] = any ? l_row : 0.f;
+            }
+        }
+        named_bar(kBarEpilogue, kSoftmaxThreads);
+        {
+            const int cpr = row_bytes / 16;  // 16-byte chunks of a row
+            for (int idx = threadIdx.x; idx < kRows * cpr; idx += kSoftmaxThreads) {
+                const int rr = idx / cpr, ch = idx - rr * cpr;
+                const int grr = rb * kRows + rr;
+                if (grr >= rows_total) continue;
+                const uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * pitch + ch * 16);
+                uint8_t *dst = p.num_splits == 1
+                    ? reinterpret_cast<uint8_t *>(p.o_lat + row_index(grr) * p.d_c + g.k0)
+                    : reinterpret_cast<uint8_t *>(p.part_acc + (((long long)b * p.num_splits + split) * rows_total + grr) * p.d_c + g.k0);
+                *reinterpret_cast<uint4 *>(dst + ch * 16) = v;
             }
         }
         tc_fence_before();
