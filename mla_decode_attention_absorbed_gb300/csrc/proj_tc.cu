@@ -9,9 +9,12 @@
 // one head, over all of K or, split K, over a run of K chunks whose fp32 tile
 // it stores as that split's partial.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads, warp 1 owns tensor memory
-// and issues the MMAs, warps 2-5 drain the fp32 accumulator from TMEM, round to
-// bf16 and store.  K is streamed in 64-wide chunks through a 4-stage ring.
+// Warp roles (320 threads): warp 0 issues TMA loads, warp 1 owns tensor memory
+// and issues the MMAs, warps 2-9 drain the fp32 accumulator from TMEM (two warps
+// per lane quadrant, one half of the columns each), round to bf16 and stage the
+// rows in the idle operand ring, then store them as whole rows (consecutive
+// lanes on consecutive 16-byte chunks).  K is streamed in 64-wide chunks through
+// a 4-stage ring.
 #include "common.cuh"
 #include "launch.h"
 #include "sm100.cuh"
@@ -25,7 +28,9 @@ using namespace sm100;
 constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = kThreads - 64;  // warps 2-9
+constexpr uint32_t kBarEpi = 1;             // named barrier of the epilogue warps
 
 struct ProjArgs {
     int M;                 // query tokens (B * s_q)
@@ -58,6 +63,7 @@ struct ProjSmem {
     static constexpr int kBBytes = BN * kBK * 2;   // 32 KB at BN = 256
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kBytes = kStagesN * kStageBytes + 1024 /* barriers */ + 1024 /* alignment */;
+    static_assert(kBM * (BN * 2 + 16) <= kStagesN * kStageBytes, "the bf16 rows are staged in the operand ring");
 };
 
 template <int BN, bool kBMN>
@@ -161,19 +167,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(acc_full);
     } else if (warp >= 2) {
-        // ---------------- epilogue: TMEM -> bf16 -> global
-        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        // ---------------- epilogue: TMEM -> bf16 -> shared staging -> global
+        const int q = warp & 3;             // TMEM lane quadrant this warp may access
+        const int c_lo = ((warp - 2) >> 2) * (BN / 2), c_hi = c_lo + BN / 2;  // its columns
         const int row = q * 32 + lane;
         const int m = m0 + row;
-        // a quadrant without a valid row (fewer than 128 tokens) has nothing to store
+        // a quadrant without a valid row (fewer than 128 tokens) has nothing to drain
         const bool live = m0 + q * 32 < g.M;
+        const int t = threadIdx.x - 64;
+        // absorb: the q_rope chunks this thread copies are read while the MMAs run
+        constexpr int kRopeMax = 4;  // 16-byte chunks per thread: 128 rows x d_rope <= 128
+        uint4 rope[kRopeMax];
+        const bool copy_rope = !g.acc && g.rope_src != nullptr && blockIdx.x == 0 && g.d_rope > 0;
+        const int rpr = copy_rope ? g.d_rope / 8 : 1;  // 16-byte chunks of a q_rope row
+        if (copy_rope) {
+#pragma unroll
+            for (int i = 0; i < kRopeMax; ++i) {
+                const int idx = t + i * kEpiThreads, rr = idx / rpr, ch = idx - rr * rpr;
+                rope[i] = make_uint4(0, 0, 0, 0);
+                if (rr < kBM && m0 + rr < g.M)
+                    rope[i] = __ldg(reinterpret_cast<const uint4 *>(g.rope_src + ((long long)(m0 + rr) * g.H + h) * g.d_rope) + ch);
+            }
+        }
         const bool ok = live && (nk <= 0 || mbar_wait(acc_full, 0)) && !*abort_flag;
         tc_fence_after();
         const int n_valid = g.N - n0;  // a multiple of 16
         if (g.acc && live) {
             // split K: this CTA's fp32 tile is split blockIdx.z's partial (zeros if it has no K)
             float *prow = g.acc + ((long long)blockIdx.z * g.M + m) * g.N + n0;
-            for (int c0 = 0; c0 < BN; c0 += 16) {
+            for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(tmem + tmem_lane_base(q) + c0, r);
                 tmem_ld_wait();
@@ -188,28 +210,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        __nv_bfloat16 *dst = g.acc ? nullptr : g.out + ((long long)m * g.H + h) * g.out_row + n0;
-        for (int c0 = 0; live && !g.acc && c0 < BN; c0 += 16) {
-            uint32_t r[16];
-            tmem_ld16(tmem + tmem_lane_base(q) + c0, r);
-            tmem_ld_wait();
-            if (m < g.M && c0 < n_valid) {
-                uint32_t pk[8];
+        if (!g.acc) {
+            // every MMA has read the ring (acc_full), so it holds the bf16 rows now;
+            // the pitch's extra 16 bytes keep the row-per-lane writes conflict-free
+            constexpr int kPitch = BN * 2 + 16;
+            // two 16-column loads in flight per wait where the half is a multiple of 32
+            constexpr int kStep = (BN / 2) % 32 == 0 ? 32 : 16;
+            for (int c0 = c_lo; live && c0 < c_hi; c0 += kStep) {
+                uint32_t r[kStep];
+                tmem_ld16(tmem + tmem_lane_base(q) + c0, *reinterpret_cast<uint32_t(*)[16]>(&r[0]));
+                if (kStep == 32) tmem_ld16(tmem + tmem_lane_base(q) + c0 + 16, *reinterpret_cast<uint32_t(*)[16]>(&r[kStep - 16]));
+                tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float lo = ok ? __uint_as_float(r[2 * e]) : __int_as_float(0x7fc00000);
-                    float hi = ok ? __uint_as_float(r[2 * e + 1]) : __int_as_float(0x7fc00000);
-                    pk[e] = pack_bf16x2(lo, hi);
+                for (int hb = 0; hb < kStep / 16; ++hb) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        float lo = ok ? __uint_as_float(r[16 * hb + 2 * e]) : __int_as_float(0x7fc00000);
+                        float hi = ok ? __uint_as_float(r[16 * hb + 2 * e + 1]) : __int_as_float(0x7fc00000);
+                        pk[e] = pack_bf16x2(lo, hi);
+                    }
+                    uint4 *d4 = reinterpret_cast<uint4 *>(smem + row * kPitch + (c0 + 16 * hb) * 2);
+                    d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
-                d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-        }
-        if (!g.acc && g.rope_src != nullptr && blockIdx.x == 0 && m < g.M) {
-            const uint4 *src = reinterpret_cast<const uint4 *>(g.rope_src + ((long long)m * g.H + h) * g.d_rope);
-            uint4 *d = reinterpret_cast<uint4 *>(g.out + ((long long)m * g.H + h) * g.out_row + g.N);
-            for (int e = 0; e < g.d_rope / 8; ++e) d[e] = src[e];
+            named_bar(kBarEpi, kEpiThreads);
+            const int cpr = min(BN, n_valid) / 8;  // 16-byte chunks of a row
+            for (int idx = t; idx < kBM * cpr; idx += kEpiThreads) {
+                const int rr = idx / cpr, ch = idx - rr * cpr;
+                if (m0 + rr >= g.M) break;  // rows only grow with idx
+                *reinterpret_cast<uint4 *>(g.out + ((long long)(m0 + rr) * g.H + h) * g.out_row + n0 + ch * 8) =
+                    *reinterpret_cast<const uint4 *>(smem + rr * kPitch + ch * 16);
+            }
+            if (copy_rope) {
+#pragma unroll
+                for (int i = 0; i < kRopeMax; ++i) {
+                    const int idx = t + i * kEpiThreads, rr = idx / rpr, ch = idx - rr * rpr;
+                    if (rr < kBM && m0 + rr < g.M)
+                        reinterpret_cast<uint4 *>(g.out + ((long long)(m0 + rr) * g.H + h) * g.out_row + g.N)[ch] = rope[i];
+                }
+            }
         }
         tc_fence_before();
     }
