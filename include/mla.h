@@ -153,7 +153,9 @@ MLA_API size_t mla_decode_workspace_size(const mla_dims *dims, const mla_cache *
                                          int num_splits);
 
 /* Split count mla_decode_attn uses for num_splits == 0 (a function of the dims,
- * B and the max_seq_len hint only).  Returns 0 for invalid arguments. */
+ * B and the max_seq_len hint only): the pieces per sequence, or, when the plan
+ * splits only the sequences of a last, partly filled wave (see mla_decode_attn),
+ * the pieces of those.  Returns 0 for invalid arguments. */
 MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
 
 /* Latent-space attention of every head against the shared latent cache
@@ -167,7 +169,12 @@ MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
  * The history of each sequence is cut into num_splits pieces processed in
  * parallel, each keeping an online softmax; the pieces are merged with a
  * log-sum-exp combine.  q_cat [B][s_q][H][d_c+d_rope]; o_lat [B][s_q][H][d_c];
- * lse fp32 [B][s_q][H].  num_splits 0 = the library's choice, else 1..64. */
+ * lse fp32 [B][s_q][H].  num_splits 0 = the library's choice, else 1..64: every
+ * sequence in num_splits pieces.  The library's choice splits every sequence
+ * while the pieces fit one wave of the GPU; with more 128-row work items than a
+ * wave holds, it leaves them whole except those of a last, partly filled wave,
+ * whose sequences (the last ones of the batch) are split to fill that wave; their
+ * pieces are the last work items of the same grid. */
 MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
                             void *o_lat, float *lse, void *workspace, size_t ws_bytes,
                             int num_splits, void *stream);

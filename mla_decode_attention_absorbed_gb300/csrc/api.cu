@@ -91,10 +91,6 @@ int plan_splits_len(const mla_dims *d, long long maxL, int requested) {
     return (int)want;
 }
 
-int plan_splits(const mla_dims *d, const mla_cache *c, int requested) {
-    return plan_splits_len(d, c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c), requested);
-}
-
 // Sparse decode: the index list must be shared by all rows of a 128-row block
 // (one query token per block, or a single query token), and the contiguous
 // cache must be a stack of whole rows (gathered through a 2-D view).
@@ -135,12 +131,83 @@ size_t expand_workspace_bytes(const mla_dims *d, const mla_cache *c) {
            (size_t)d->B * d->H * (size_t)cache_capacity(c) * (size_t)expanded_width(d) * 2;
 }
 
+// Work plan of a dense decode attention: sequences [0, B - b_tail) run in
+// `splits` pieces each, the last b_tail sequences in tail_splits pieces.
+struct DecodePlan {
+    int splits;
+    int b_tail;
+    int tail_splits;
+};
+
+// The library's plan (requested == 0), else `requested` pieces for every
+// sequence.  When the work items (sequence x 128-row block) fill more than one
+// wave of clusters and the last wave is only partly used, the sequences of that
+// last wave are split over the whole of it instead: the ones before run unsplit
+// and write their rows directly, and only the tail's pieces are merged.  The
+// wave arithmetic assumes sequences of about equal length (only max_seq_len is
+// known here); with ragged lengths the tail's pieces simply start as slots free.
+DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
+    const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
+    DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1};
+    if (requested > 0 || pl.splits > 1) return pl;
+    const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
+    const long long units = (long long)d->B * row_blocks;
+    const long long slots = d->d_c > 256 ? kNumSMs / 2 : kNumSMs;
+    const long long rem = units % slots;
+    if (units <= slots || rem == 0) return pl;
+    const long long b_tail = (rem + row_blocks - 1) / row_blocks;
+    if (b_tail >= d->B) return pl;
+    long long k = slots / (b_tail * row_blocks);
+    const long long cap = ((maxL + 63) / 64) / 8;  // pieces of at least 8 tiles
+    if (k > cap) k = cap;
+    if (k > kMaxSplits) k = kMaxSplits;
+    if (k < 2) return pl;
+    pl.b_tail = (int)b_tail;
+    pl.tail_splits = (int)k;
+    return pl;
+}
+
+// Status word, then the split pieces' partials (only the tail's, if the plan has one).
+size_t plan_workspace_bytes(const mla_dims *d, const DecodePlan &pl) {
+    if (pl.b_tail == 0) return attn_workspace_bytes(d, pl.splits);
+    mla_dims t = *d;
+    t.B = pl.b_tail;
+    return attn_workspace_bytes(&t, pl.tail_splits);
+}
+
 // absorbed prefill: the attention's own workspace first (so that the status word
 // sits at the start, as for every entry point), then q_cat and o_lat
-size_t absorbed_workspace_bytes(const mla_dims *d, int splits) {
+size_t absorbed_workspace_bytes(const mla_dims *d, size_t attn_ws) {
     const size_t rows = (size_t)d->B * d->s_q * d->H;
-    return round_up(attn_workspace_bytes(d, splits), 256) + round_up(rows * (d->d_c + d->d_rope) * 2, 256) +
-           rows * d->d_c * 2;
+    return round_up(attn_ws, 256) + round_up(rows * (d->d_c + d->d_rope) * 2, 256) + rows * d->d_c * 2;
+}
+
+// Points p's split partials into the workspace, for nb sequences in `splits` pieces.
+void set_partials(mla::AttnParams &p, const mla_dims *d, int nb, int splits, void *workspace) {
+    p.num_splits = splits;
+    if (splits > 1) {
+        const size_t rows = (size_t)nb * splits * d->s_q * d->H;
+        char *base = (char *)workspace + kStatusBytes;
+        p.part_ml = (float *)base;
+        p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
+    }
+}
+
+// The attention launch of plan pl (and the merge of split pieces); p carries the
+// whole batch.  A tail is one grid with the rest: its pieces are the grid's last
+// work items, so the hardware starts them as the whole sequences before them
+// leave the SMs, and only they are merged.
+cudaError_t launch_decode_plan(const mla_dims *d, const DecodePlan &pl, mla::AttnParams p, void *workspace,
+                               cudaStream_t st) {
+    if (pl.b_tail == 0) {
+        set_partials(p, d, d->B, pl.splits, workspace);
+        return mla::launch_attn_tc(p, st);
+    }
+    set_partials(p, d, pl.b_tail, pl.tail_splits, workspace);
+    p.num_splits = 1;
+    p.tail_b0 = d->B - pl.b_tail;
+    p.tail_splits = pl.tail_splits;
+    return mla::launch_attn_tc(p, st);
 }
 
 mla::AttnParams make_params(const mla_dims *d, const mla_cache *c) {
@@ -194,13 +261,14 @@ MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q
 
 MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache) {
     if (check_dims(dims) || check_cache(dims, cache)) return 0;
-    return plan_splits(dims, cache, 0);
+    const DecodePlan pl = plan_decode(dims, cache, 0);
+    return pl.b_tail ? pl.tail_splits : pl.splits;
 }
 
 MLA_API size_t mla_decode_workspace_size(const mla_dims *dims, const mla_cache *cache, int num_splits) {
     if (check_dims(dims) || check_cache(dims, cache)) return 0;
     if (num_splits < 0 || num_splits > kMaxSplits) return 0;
-    return attn_workspace_bytes(dims, plan_splits(dims, cache, num_splits));
+    return plan_workspace_bytes(dims, plan_decode(dims, cache, num_splits));
 }
 
 MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_cache *cache, void *o_lat,
@@ -212,8 +280,8 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
     if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
-    const int splits = plan_splits(dims, cache, num_splits);
-    if (ws_bytes < attn_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    const DecodePlan pl = plan_decode(dims, cache, num_splits);
+    if (ws_bytes < plan_workspace_bytes(dims, pl)) return MLA_ERR_WORKSPACE;
     if (dims->B > 0) {
         if (!q_cat || !o_lat || !lse) return MLA_ERR_NULL;
         if (!aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse)) return MLA_ERR_ALIGN;
@@ -226,15 +294,8 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
     p.q_cat = (const __nv_bfloat16 *)q_cat;
     p.o_lat = (__nv_bfloat16 *)o_lat;
     p.lse = lse;
-    p.num_splits = splits;
     p.status = (int *)workspace;
-    if (splits > 1) {
-        size_t rows = (size_t)dims->B * splits * dims->s_q * dims->H;
-        char *base = (char *)workspace + kStatusBytes;
-        p.part_ml = (float *)base;
-        p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
-    }
-    cudaError_t e = mla::launch_attn_tc(p, st);
+    cudaError_t e = launch_decode_plan(dims, pl, p, workspace, st);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -424,7 +485,7 @@ MLA_API int mla_prefill_expand(const mla_dims *dims, const void *q_nope, const v
 
 MLA_API size_t mla_prefill_workspace_size(const mla_dims *dims, const mla_cache *cache) {
     if (check_shape(dims) || check_cache(dims, cache)) return 0;
-    size_t n = check_dims(dims) ? 0 : absorbed_workspace_bytes(dims, plan_splits(dims, cache, 0));
+    size_t n = check_dims(dims) ? 0 : absorbed_workspace_bytes(dims, plan_workspace_bytes(dims, plan_decode(dims, cache, 0)));
     if (!check_expand(dims, cache)) {
         const size_t e = expand_workspace_bytes(dims, cache);
         if (e > n) n = e;
@@ -444,18 +505,16 @@ MLA_API int mla_prefill(const mla_dims *dims, const void *q_nope, const void *q_
     if (path) *path = expand ? MLA_PATH_EXPAND : MLA_PATH_ABSORB;
     if (expand) return mla_prefill_expand(dims, q_nope, q_rope, cache, w_uk, w_uv, out, lse, workspace, ws_bytes, stream);
     if ((s = check_dims(dims))) return s;
-    const int splits = plan_splits(dims, cache, 0);
+    const size_t attn_ws_bytes = plan_workspace_bytes(dims, plan_decode(dims, cache, 0));
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
-    if (ws_bytes < absorbed_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    if (ws_bytes < absorbed_workspace_bytes(dims, attn_ws_bytes)) return MLA_ERR_WORKSPACE;
     const size_t rows = (size_t)dims->B * dims->s_q * dims->H;
     char *attn_ws = (char *)workspace;
-    char *q_cat = attn_ws + round_up(attn_workspace_bytes(dims, splits), 256);
+    char *q_cat = attn_ws + round_up(attn_ws_bytes, 256);
     char *o_lat = q_cat + round_up(rows * (dims->d_c + dims->d_rope) * 2, 256);
     if ((s = mla_absorb_q(dims, q_nope, q_rope, w_uk, q_cat, stream))) return s;
-    if ((s = mla_decode_attn(dims, q_cat, cache, o_lat, lse, attn_ws, attn_workspace_bytes(dims, splits), splits,
-                             stream)))
-        return s;
+    if ((s = mla_decode_attn(dims, q_cat, cache, o_lat, lse, attn_ws, attn_ws_bytes, 0, stream))) return s;
     return mla_out_proj(dims, o_lat, w_uv, out, stream);
 }
 
@@ -469,8 +528,8 @@ MLA_API int mla_decode_step(const mla_dims *dims, const void *q_nope, const void
     if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
-    const int splits = plan_splits(dims, cache, num_splits);
-    if (ws_bytes < attn_workspace_bytes(dims, splits)) return MLA_ERR_WORKSPACE;
+    const DecodePlan pl = plan_decode(dims, cache, num_splits);
+    if (ws_bytes < plan_workspace_bytes(dims, pl)) return MLA_ERR_WORKSPACE;
     if (dims->B > 0) {
         if (!q_nope || !w_uk || !w_uv || !q_cat || !o_lat || !out || !lse || (dims->d_rope && !q_rope))
             return MLA_ERR_NULL;
@@ -490,16 +549,9 @@ MLA_API int mla_decode_step(const mla_dims *dims, const void *q_nope, const void
     p.q_cat = (const __nv_bfloat16 *)q_cat;
     p.o_lat = (__nv_bfloat16 *)o_lat;
     p.lse = lse;
-    p.num_splits = splits;
     p.status = (int *)workspace;
     p.pdl = 1;
-    if (splits > 1) {
-        size_t rows = (size_t)dims->B * splits * dims->s_q * dims->H;
-        char *base = (char *)workspace + kStatusBytes;
-        p.part_ml = (float *)base;
-        p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
-    }
-    if ((e = mla::launch_attn_tc(p, st)) != cudaSuccess) return MLA_ERR_CUDA;
+    if ((e = launch_decode_plan(dims, pl, p, workspace, st)) != cudaSuccess) return MLA_ERR_CUDA;
     e = mla::launch_out_proj_tc(*dims, o_lat, w_uv, out, st, true);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -326,7 +326,16 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     const Geo g = rank == 0 ? g0 : g1;
     const CUtensorMap *tm = rank == 0 ? &tm0 : &tm1;
     const int rb = kSplit ? blockIdx.x / 2 : blockIdx.x;
-    const int split = blockIdx.y, b = blockIdx.z;
+    // work item -> sequence, piece of it and the sequence's piece count; part_seq
+    // indexes the sequence's partials
+    int split = blockIdx.y, b = blockIdx.z, nsplit = p.num_splits, part_seq = blockIdx.z;
+    if (p.tail_splits > 1 && b >= p.tail_b0) {
+        const int i = b - p.tail_b0;
+        nsplit = p.tail_splits;
+        split = i % nsplit;
+        part_seq = i / nsplit;
+        b = p.tail_b0 + part_seq;
+    }
     const int rows_total = p.s_q * p.H;
     // expanded attention: work-item sequence b is head hsub of sequence bseq
     const int hps = p.heads_per_seq > 1 ? p.heads_per_seq : 1;
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     const bool seq_ok = seq_len_ok(p, L);
     // [t0, t1): token positions (dense) or positions in the sparse list
     int t0 = 0, t1 = 0;
-    if (seq_ok) split_range(kSparse ? p.topk : L, p.num_splits, split, t0, t1);
+    if (seq_ok) split_range(kSparse ? p.topk : L, nsplit, split, t0, t1);
     if (!kSparse && seq_ok) {
         // no row of this block sees a token past its last query's causal limit:
         // those tiles are not streamed at all (with many new tokens -- a prefill --
@@ -1030,9 +1039,9 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         // the softmax warps store whole rows, consecutive lanes on consecutive 16-byte
         // chunks, instead of one 16-byte piece of 32 different rows per instruction.
         uint8_t *stg = &sm.kv[0][0];
-        const int eb = p.num_splits == 1 ? 2 : 4;  // bf16 output or fp32 partial
+        const int eb = nsplit == 1 ? 2 : 4;  // bf16 output or fp32 partial
         const int row_bytes = g.vn * eb, pitch = row_bytes + 16;
-        if (p.num_splits == 1) {
+        if (nsplit == 1) {
             const float inv = any ? vscale / l_row : 0.f;
             for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
@@ -1050,7 +1059,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             if (store && rank == 0 && hf == 0)
                 p.lse[row_index(gr)] = any ? (m2 + __log2f(l_row)) * ln2 : -INFINITY;
         } else {
-            const long long prow = ((long long)b * p.num_splits + split) * rows_total + gr;
+            const long long prow = ((long long)part_seq * nsplit + split) * rows_total + gr;
             for (int c = half_cols * hf; c < half_cols * (hf + 1); c += 16) {
                 uint32_t u[16];
                 tmem_ld16(tmem + lane_base + kColO + c, u);
@@ -1076,9 +1085,9 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                 const int grr = rb * kRows + rr;
                 if (grr >= rows_total) continue;
                 const uint4 v = *reinterpret_cast<const uint4 *>(stg + rr * pitch + ch * 16);
-                uint8_t *dst = p.num_splits == 1
+                uint8_t *dst = nsplit == 1
                     ? reinterpret_cast<uint8_t *>(p.o_lat + row_index(grr) * p.d_c + g.k0)
-                    : reinterpret_cast<uint8_t *>(p.part_acc + (((long long)b * p.num_splits + split) * rows_total + grr) * p.d_c + g.k0);
+                    : reinterpret_cast<uint8_t *>(p.part_acc + (((long long)part_seq * nsplit + split) * rows_total + grr) * p.d_c + g.k0);
                 *reinterpret_cast<uint4 *>(dst + ch * 16) = v;
             }
         }
@@ -1140,7 +1149,8 @@ cudaError_t launch_variant(const CUtensorMap &tm0, const CUtensorMap &tm1, const
     }
     const int row_blocks = (p.s_q * p.H + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(row_blocks * (kSplit ? 2 : 1), p.num_splits, p.B);
+    const int items = p.tail_splits > 1 ? p.tail_b0 + (p.B - p.tail_b0) * p.tail_splits : p.B;
+    cfg.gridDim = dim3(row_blocks * (kSplit ? 2 : 1), p.tail_splits > 1 ? 1 : p.num_splits, items);
     cfg.blockDim = dim3(threads_of(kSparse, kFp8));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -1268,7 +1278,18 @@ cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
         tm1 = tm0;
     }
     cudaError_t e = split ? launch_split<true>(tm0, tm1, p, g0, g1, st) : launch_split<false>(tm0, tm1, p, g0, g1, st);
-    if (e != cudaSuccess || p.num_splits == 1) return e;
+    if (e != cudaSuccess) return e;
+    if (p.tail_splits > 1) {
+        // merge the tail's pieces: its sequences as a batch of their own
+        AttnParams t = p;
+        const long long rows0 = (long long)p.tail_b0 * p.s_q * p.H;
+        t.B = p.B - p.tail_b0;
+        t.num_splits = p.tail_splits;
+        t.o_lat = p.o_lat + rows0 * p.d_c;
+        t.lse = p.lse + rows0;
+        return launch_attn_combine(t, st);
+    }
+    if (p.num_splits == 1) return e;
     return launch_attn_combine(p, st);
 }
 

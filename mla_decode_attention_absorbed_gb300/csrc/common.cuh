@@ -25,6 +25,11 @@ struct AttnParams {
     __nv_bfloat16 *o_lat;         // [B][s_q][H][d_c]
     float *lse;                   // [B][s_q][H]
     int num_splits;
+    // tail pieces (tail_splits > 1, with num_splits == 1): grid items below tail_b0
+    // are whole sequences, item tail_b0 + i is piece i % tail_splits of sequence
+    // tail_b0 + i / tail_splits; partials are kept for those sequences only,
+    // indexed from tail_b0
+    int tail_b0, tail_splits;
     float *part_acc;              // [B][splits][s_q*H][d_c] (num_splits > 1)
     float *part_ml;               // [B][splits][s_q*H][2 CTA halves][2]   (m, l)
     int *status;                  // device status word

@@ -54,8 +54,8 @@ MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, con
     if (num_splits < 0) return MLA_ERR_SHAPE;
     if (device_status && ((uintptr_t)device_status & 3u)) return MLA_ERR_ALIGN;
     int splits = num_splits;
-    if (splits == 0) {
-        // The library's own choice when its partials fit, else the largest count that fits.
+    if (splits == 0 && mla_decode_workspace_size(dims, cache, 0) > kStaticScratchBytes) {
+        // The library's own plan when its partials fit, else the largest uniform count that fits.
         splits = mla_decode_num_splits(dims, cache);
         if (splits == 0) {  // the checks below report why the arguments are invalid
             splits = 1;

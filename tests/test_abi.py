@@ -103,6 +103,29 @@ def test_workspace_and_split_queries(lib):
     assert naive >= 64 * 128 * 4096 * 256 * 2
 
 
+def test_tail_plan_fills_the_last_wave(lib):
+    """More 128-row work items than a wave of 76 clusters holds: the plan leaves
+    them whole except the sequences of the partly filled last wave, which it
+    splits, and the workspace holds only their partials."""
+    d = dsv3(B=64, s_q=4).dims()  # 256 work items = 3 waves + 28
+    c = fake_cache(8192)
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 2  # 76 // 28
+    tail_rows = 7 * 2 * 4 * 128  # the last 7 sequences, 2 pieces, 512 rows each
+    need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 0)
+    assert tail_rows * 512 * 4 <= need < 2 * tail_rows * 512 * 4
+    # an explicit count splits every sequence
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 2) >= 64 * 2 * 512 * 512 * 4
+    # whole waves, or one wave, keep the plain plan
+    d = dsv3(B=76, s_q=1).dims()
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 0) < 4096
+    d = dsv3(B=64, s_q=1).dims()
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
+    # pieces stay at least 8 tiles long: a 1024-token history allows 2 pieces
+    d = dsv3(B=20, s_q=4).dims()  # 80 work items: one sequence in the last wave
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(fake_cache(1024))) == 2
+
+
 def test_prefill_crossover_matches_the_pages_formula(lib):
     """The library's dispatch point (host code) against the oracle's counter, which
     the page figures pin (S* = 128 at L = 512, 170 at 32K, 171 at 128K)."""

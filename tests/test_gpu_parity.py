@@ -147,6 +147,37 @@ def test_full_size_sampled(name):
         assert torch.isfinite(g[k].float()).all(), k
 
 
+def test_tail_plan_matches_unsplit_and_oracle():
+    """80 work items on 76 cluster slots: the last sequence runs in two pieces (the
+    grid's last work items, merged), the others unsplit; the result agrees with
+    the unsplit launch and the oracle, and the fused step with the same plan is
+    bit-identical."""
+    from helpers import sample_rows
+    cfg = MLAConfig("tail", B=20, s_q=4, T=1024, seed=61, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    d = to_dev(inp)
+    prob, cache = gpu_cache(cfg, d)
+    assert mla.decode_num_splits(prob, cache) == 2
+    auto = run_gpu(cfg, inp)
+    one = run_gpu(cfg, inp, num_splits=1)
+    assert auto["status"] == 0 and one["status"] == 0
+    within_tolerance(auto["o_lat"].double(), one["o_lat"].double(), "tail plan vs unsplit o_lat")
+    within_tolerance(auto["lse"].double(), one["lse"].double(), "tail plan vs unsplit lse")
+    # the head sequences run exactly as in the unsplit launch
+    head = (cfg.B - 1) * cfg.s_q * cfg.H
+    assert torch.equal(auto["o_lat"].view(-1, cfg.d_c)[:head], one["o_lat"].view(-1, cfg.d_c)[:head])
+    tail_rows = list(range(head, head + cfg.s_q * cfg.H, 37)) + [cfg.B * cfg.s_q * cfg.H - 1]
+    check_against_oracle(cfg, inp, auto, rows=sorted(set(sample_rows(cfg, 16) + tail_rows)))
+    dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], cfg.page_size)
+    out_f = dec.step(d["q_nope"], d["q_rope"]).clone()
+    lse_f = dec.lse.clone()
+    out_s = dec(d["q_nope"], d["q_rope"]).clone()
+    torch.cuda.synchronize()
+    assert mla.read_status(dec.workspace) == 0
+    assert torch.equal(out_f, out_s) and torch.equal(lse_f, dec.lse)
+    assert torch.equal(lse_f.cpu(), auto["lse"])
+
+
 # ---------------------------------------------------------------- naive comparison path
 def _run_naive(cfg, inp):
     d = to_dev(inp)
