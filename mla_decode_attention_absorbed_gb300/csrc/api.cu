@@ -13,6 +13,7 @@ constexpr int kAbiVersion = 2;
 constexpr int kMaxSplits = 64;
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (split planning only)
 constexpr size_t kStatusBytes = 256;  // status word + padding at the workspace start
+constexpr int kMaxOrdered = 1024;     // longest-first work order up to this many sequences
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -137,6 +138,7 @@ struct DecodePlan {
     int splits;
     int b_tail;
     int tail_splits;
+    bool lpt;  // longest sequences first (several waves of whole sequences)
 };
 
 // The library's plan (requested == 0), else `requested` pieces for every
@@ -146,13 +148,18 @@ struct DecodePlan {
 // and write their rows directly, and only the tail's pieces are merged.  The
 // wave arithmetic assumes sequences of about equal length (only max_seq_len is
 // known here); with ragged lengths the tail's pieces simply start as slots free.
+// Over several waves of whole sequences the work order is longest first (the
+// kernel ranks the lengths, which only the device knows; up to 1024 sequences,
+// bf16 caches), so that a long sequence does not start in the last wave; with
+// equal lengths the order is the batch order.
 DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
     const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
-    DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1};
-    if (requested > 0 || pl.splits > 1) return pl;
+    DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1, false};
     const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
     const long long units = (long long)d->B * row_blocks;
     const long long slots = d->d_c > 256 ? kNumSMs / 2 : kNumSMs;
+    pl.lpt = pl.splits == 1 && units > slots && d->B <= kMaxOrdered && c->kv_dtype == MLA_KV_BF16;
+    if (requested > 0 || pl.splits > 1) return pl;
     const long long rem = units % slots;
     if (units <= slots || rem == 0) return pl;
     const long long b_tail = (rem + row_blocks - 1) / row_blocks;
@@ -167,12 +174,18 @@ DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
     return pl;
 }
 
-// Status word, then the split pieces' partials (only the tail's, if the plan has one).
+// Bytes of the work order (sequence of each work-order position) after the status word.
+size_t order_bytes(const mla_dims *d, const DecodePlan &pl) {
+    return pl.lpt ? round_up((size_t)d->B * sizeof(int), 256) : 0;
+}
+
+// Status word, the work order, then the split pieces' partials (only the tail's,
+// if the plan has one).
 size_t plan_workspace_bytes(const mla_dims *d, const DecodePlan &pl) {
-    if (pl.b_tail == 0) return attn_workspace_bytes(d, pl.splits);
+    if (pl.b_tail == 0) return attn_workspace_bytes(d, pl.splits) + order_bytes(d, pl);
     mla_dims t = *d;
     t.B = pl.b_tail;
-    return attn_workspace_bytes(&t, pl.tail_splits);
+    return attn_workspace_bytes(&t, pl.tail_splits) + order_bytes(d, pl);
 }
 
 // absorbed prefill: the attention's own workspace first (so that the status word
@@ -182,12 +195,13 @@ size_t absorbed_workspace_bytes(const mla_dims *d, size_t attn_ws) {
     return round_up(attn_ws, 256) + round_up(rows * (d->d_c + d->d_rope) * 2, 256) + rows * d->d_c * 2;
 }
 
-// Points p's split partials into the workspace, for nb sequences in `splits` pieces.
-void set_partials(mla::AttnParams &p, const mla_dims *d, int nb, int splits, void *workspace) {
+// Points p's split partials into the workspace (past `skip` bytes of work order),
+// for nb sequences in `splits` pieces.
+void set_partials(mla::AttnParams &p, const mla_dims *d, int nb, int splits, void *workspace, size_t skip = 0) {
     p.num_splits = splits;
     if (splits > 1) {
         const size_t rows = (size_t)nb * splits * d->s_q * d->H;
-        char *base = (char *)workspace + kStatusBytes;
+        char *base = (char *)workspace + kStatusBytes + skip;
         p.part_ml = (float *)base;
         p.part_acc = (float *)(base + round_up(rows * 4 * sizeof(float), 256));
     }
@@ -199,11 +213,16 @@ void set_partials(mla::AttnParams &p, const mla_dims *d, int nb, int splits, voi
 // leave the SMs, and only they are merged.
 cudaError_t launch_decode_plan(const mla_dims *d, const DecodePlan &pl, mla::AttnParams p, void *workspace,
                                cudaStream_t st) {
+    const size_t ob = order_bytes(d, pl);
+    if (pl.lpt) {
+        p.lpt = 1;
+        p.order = (int *)((char *)workspace + kStatusBytes);
+    }
     if (pl.b_tail == 0) {
-        set_partials(p, d, d->B, pl.splits, workspace);
+        set_partials(p, d, d->B, pl.splits, workspace, ob);
         return mla::launch_attn_tc(p, st);
     }
-    set_partials(p, d, pl.b_tail, pl.tail_splits, workspace);
+    set_partials(p, d, pl.b_tail, pl.tail_splits, workspace, ob);
     p.num_splits = 1;
     p.tail_b0 = d->B - pl.b_tail;
     p.tail_splits = pl.tail_splits;

@@ -146,6 +146,7 @@ struct Smem {
     uint64_t staged, tx_free, rx_full[2];
     uint32_t tmem_base;
     int abort;    // set by this CTA or, remotely, by the peer
+    int lpt_b, lpt_L;  // longest-first order: the sequence of this CTA's work item, its length
     int armed;    // last tile whose receive the exchange warp armed
     int received; // last tile the softmax warps received
 };
@@ -336,25 +337,21 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         part_seq = i / nsplit;
         b = p.tail_b0 + part_seq;
     }
-    const int rows_total = p.s_q * p.H;
+    // longest-first order (dense bf16 variants only: compiled into the 512-thread
+    // FP8 kernel it cost 3 %): every length is requested now and used after the
+    // setup below, which hides the load
+    constexpr bool kOrdered = !kFp8 && !kSparse;
+    const bool lpt = kOrdered && p.lpt;
+    constexpr int kLensPerThread = 3;  // 3 x 384 threads >= 1024 sequences
+    int lens_reg[kLensPerThread];
+#pragma unroll
+    for (int k = 0; k < kLensPerThread; ++k) {
+        const int c = threadIdx.x + k * blockDim.x;
+        lens_reg[k] = lpt && c < p.B ? __ldg(p.seq_lens + c) : 0;
+    }
     // expanded attention: work-item sequence b is head hsub of sequence bseq
     const int hps = p.heads_per_seq > 1 ? p.heads_per_seq : 1;
-    const int bseq = b / hps, hsub = b % hps;
-    auto row_index = [&](int gr) -> long long { return ((long long)bseq * rows_total + gr) * hps + hsub; };
-
-    const int L = __ldg(p.seq_lens + bseq);
-    const bool seq_ok = seq_len_ok(p, L);
-    // [t0, t1): token positions (dense) or positions in the sparse list
-    int t0 = 0, t1 = 0;
-    if (seq_ok) split_range(kSparse ? p.topk : L, nsplit, split, t0, t1);
-    if (!kSparse && seq_ok) {
-        // no row of this block sees a token past its last query's causal limit:
-        // those tiles are not streamed at all (with many new tokens -- a prefill --
-        // this halves the work)
-        const int q_last = min(p.s_q - 1, ((rb + 1) * kRows - 1) / p.H);
-        t1 = max(t0, min(t1, L - p.s_q + q_last + 1));
-    }
-    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    const int L_pre = lpt ? 0 : __ldg(p.seq_lens + b / hps);  // the sequence's length, likewise early
 
     if (threadIdx.x == 0) {
         // the loaders of a CTA whose slice has no box past the gathered ones stay idle
@@ -386,13 +383,56 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         tma_prefetch_desc(&tm0);
         if (kSplit) tma_prefetch_desc(&tm1);
     }
-    if (!seq_ok && split == 0 && rb == 0 && rank == 0 && threadIdx.x == 0) set_status(p.status, MLA_ERR_SEQLEN);
     if (warp == kMma) tmem_alloc<512>(&sm.tmem_base);
     tc_fence_before();
     if (kSplit) cluster_sync();
     else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    if (lpt) {
+        // longest first: position b of the work order is the sequence of rank b by
+        // (length descending, index ascending), so that over several waves the long
+        // sequences start first and the short ones fill in behind them; every CTA
+        // ranks the lengths itself (B is small: the host enables this up to 1024)
+        int *lens = reinterpret_cast<int *>(sm.tx);
+#pragma unroll
+        for (int k = 0; k < kLensPerThread; ++k) {
+            const int c = threadIdx.x + k * blockDim.x;
+            if (c < p.B) lens[c] = lens_reg[k];
+        }
+        __syncthreads();
+        for (int c = threadIdx.x; c < p.B; c += blockDim.x) {
+            const int lc = lens[c];
+            int r = 0;
+            for (int d = 0; d < p.B; ++d) r += (lens[d] > lc) || (lens[d] == lc && d < c);
+            if (r == b) {
+                sm.lpt_b = c;
+                sm.lpt_L = lc;
+            }
+        }
+        __syncthreads();
+        // the merge of split pieces finds a position's sequence here
+        if (p.order != nullptr && threadIdx.x == 0 && rb == 0 && split == 0 && rank == 0) p.order[b] = sm.lpt_b;
+        b = sm.lpt_b;
+    }
+    const int rows_total = p.s_q * p.H;
+    const int bseq = b / hps, hsub = b % hps;
+    auto row_index = [&](int gr) -> long long { return ((long long)bseq * rows_total + gr) * hps + hsub; };
+
+    const int L = lpt ? sm.lpt_L : L_pre;
+    const bool seq_ok = seq_len_ok(p, L);
+    // [t0, t1): token positions (dense) or positions in the sparse list
+    int t0 = 0, t1 = 0;
+    if (seq_ok) split_range(kSparse ? p.topk : L, nsplit, split, t0, t1);
+    if (!kSparse && seq_ok) {
+        // no row of this block sees a token past its last query's causal limit:
+        // those tiles are not streamed at all (with many new tokens -- a prefill --
+        // this halves the work)
+        const int q_last = min(p.s_q - 1, ((rb + 1) * kRows - 1) / p.H);
+        t1 = max(t0, min(t1, L - p.s_q + q_last + 1));
+    }
+    const int ntiles = (t1 - t0 + kTile - 1) / kTile;
+    if (!seq_ok && split == 0 && rb == 0 && rank == 0 && threadIdx.x == 0) set_status(p.status, MLA_ERR_SEQLEN);
 
     if (warp >= kSoftmaxWarps) {
         if constexpr (kRegSplit) regs_dec<kRegOther>();
@@ -1280,13 +1320,12 @@ cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st) {
     cudaError_t e = split ? launch_split<true>(tm0, tm1, p, g0, g1, st) : launch_split<false>(tm0, tm1, p, g0, g1, st);
     if (e != cudaSuccess) return e;
     if (p.tail_splits > 1) {
-        // merge the tail's pieces: its sequences as a batch of their own
+        // merge the tail's pieces: work-order positions tail_b0.. (their sequences
+        // through p.order when the order is longest first)
         AttnParams t = p;
-        const long long rows0 = (long long)p.tail_b0 * p.s_q * p.H;
         t.B = p.B - p.tail_b0;
         t.num_splits = p.tail_splits;
-        t.o_lat = p.o_lat + rows0 * p.d_c;
-        t.lse = p.lse + rows0;
+        t.combine_b0 = p.tail_b0;
         return launch_attn_combine(t, st);
     }
     if (p.num_splits == 1) return e;

@@ -12,8 +12,12 @@ namespace mla {
 
 __global__ void attn_combine(AttnParams p) {
     const int rows = p.s_q * p.H;
-    const long long grow = blockIdx.x;
-    const int b = (int)(grow / rows), rr = (int)(grow % rows);
+    // partial sequence b (its pieces' rows) and the sequence bo it belongs to
+    const int b = (int)(blockIdx.x / rows), rr = (int)(blockIdx.x % rows);
+    const int pos = p.combine_b0 + b;
+    const int bo = p.order != nullptr ? p.order[pos] : pos;
+    if (bo < 0 || bo >= p.combine_b0 + p.B) return;  // positions and sequences are both 0 .. B-1
+    const long long grow = (long long)bo * rows + rr;
     const int S = p.num_splits;
     // columns [0, 256) are relative to the (m, l) of half 0, the rest to half 1
     const int halves = p.d_c > 256 ? 2 : 1;

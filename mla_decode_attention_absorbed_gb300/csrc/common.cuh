@@ -30,6 +30,13 @@ struct AttnParams {
     // tail_b0 + i / tail_splits; partials are kept for those sequences only,
     // indexed from tail_b0
     int tail_b0, tail_splits;
+    // longest-first work order (dense decode over several waves): work-order
+    // position i runs the sequence of rank i by length; order[i] records it for
+    // the merge (workspace, B ints)
+    int lpt;
+    int *order;
+    // merge: partial sequence j is work-order position combine_b0 + j
+    int combine_b0;
     float *part_acc;              // [B][splits][s_q*H][d_c] (num_splits > 1)
     float *part_ml;               // [B][splits][s_q*H][2 CTA halves][2]   (m, l)
     int *status;                  // device status word

@@ -178,6 +178,38 @@ def test_tail_plan_matches_unsplit_and_oracle():
     assert torch.equal(lse_f.cpu(), auto["lse"])
 
 
+def test_longest_first_order_ragged():
+    """100 ragged sequences on 76 cluster slots: the work order is longest first
+    (ranked on the device) and the 24 shortest sequences, the last wave, run in 3
+    pieces each; whole sequences match the explicit unsplit launch bit for bit,
+    everything matches the oracle, and the fused step is bit-identical."""
+    from helpers import sample_rows
+    cfg = MLAConfig("lpt", B=100, s_q=1, len_lo=64, len_hi=2048, paged=True, seed=62, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    d = to_dev(inp)
+    prob, cache = gpu_cache(cfg, d)
+    assert mla.decode_num_splits(prob, cache) == 3
+    auto = run_gpu(cfg, inp)
+    one = run_gpu(cfg, inp, num_splits=1)
+    assert auto["status"] == 0 and one["status"] == 0
+    within_tolerance(auto["o_lat"].double(), one["o_lat"].double(), "longest first + tail vs unsplit o_lat")
+    lens = inp["seq_lens"].tolist()
+    order = sorted(range(cfg.B), key=lambda b: (-lens[b], b))
+    rows = cfg.s_q * cfg.H
+    for b in order[:76]:  # whole sequences
+        assert torch.equal(auto["o_lat"].view(cfg.B, -1)[b], one["o_lat"].view(cfg.B, -1)[b]), b
+    split_rows = [b * rows + r for b in order[76:] for r in (0, rows - 1)]
+    check_against_oracle(cfg, inp, auto, rows=sorted(set(sample_rows(cfg, 16) + split_rows)))
+    dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], cfg.page_size)
+    out_f = dec.step(d["q_nope"], d["q_rope"]).clone()
+    lse_f = dec.lse.clone()
+    out_s = dec(d["q_nope"], d["q_rope"]).clone()
+    torch.cuda.synchronize()
+    assert mla.read_status(dec.workspace) == 0
+    assert torch.equal(out_f, out_s) and torch.equal(lse_f, dec.lse)
+    assert torch.equal(lse_f.cpu(), auto["lse"])
+
+
 # ---------------------------------------------------------------- naive comparison path
 def _run_naive(cfg, inp):
     d = to_dev(inp)
