@@ -174,7 +174,10 @@ MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
  * while the pieces fit one wave of the GPU; with more 128-row work items than a
  * wave holds, it leaves them whole except those of a last, partly filled wave,
  * whose sequences (the last ones of the batch) are split to fill that wave; their
- * pieces are the last work items of the same grid. */
+ * pieces are the last work items of the same grid.  With a bf16 cache, up to
+ * 1024 sequences and more than one wave, the work order is longest sequence
+ * first (ties by index), ranked on the device from seq_lens; the "last"
+ * sequences above are then the shortest.  Results do not depend on the order. */
 MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
                             void *o_lat, float *lse, void *workspace, size_t ws_bytes,
                             int num_splits, void *stream);
