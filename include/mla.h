@@ -177,7 +177,8 @@ MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
  * pieces are the last work items of the same grid.  With a bf16 cache, up to
  * 1024 sequences and more than one wave, the work order is longest sequence
  * first (ties by index), ranked on the device from seq_lens; the "last"
- * sequences above are then the shortest.  Results do not depend on the order. */
+ * sequences above are then the shortest.  A sequence's result depends only on
+ * how many pieces it runs in, not on its place in the order. */
 MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_cache *cache,
                             void *o_lat, float *lse, void *workspace, size_t ws_bytes,
                             int num_splits, void *stream);
