@@ -273,89 +273,29 @@ def run_ours(cfg, args, rank, world, local, active):
     attn_avg = sum(attn_ms) / K
 
     # end to end through the public API: every step copies its inputs from pinned host
-    # memory (queries, lengths, block table) and reads its result back.  Two sets of
-    # device buffers alternate: a copy stream moves step i+1's inputs in and step i-1's
-    # result out while the compute stream runs step i, as a serving loop would.
+    # memory (queries, lengths, block table) and reads its result back
     h_qn = inp["q_nope"].pin_memory()
     h_qr = inp["q_rope"].pin_memory()
     h_lens = inp["seq_lens"].pin_memory()
     h_bt = inp["block_table"].pin_memory() if inp["block_table"] is not None else None
+    host_in = [h_qn, h_qr, h_lens] + ([h_bt] if h_bt is not None else [])
     sets = []
     for j in range(2):
         lens_j = d["seq_lens"].clone()
         bt_j = d["block_table"].clone() if d["block_table"] is not None else None
         dec_j = mla.Decoder(prob, d["kv"], lens_j, d["w_uk"], d["w_uv"], bt_j, c.page_size,
                             max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=kv_scale)
-        sets.append(dict(dec=dec_j, lens=lens_j, bt=bt_j, qn=torch.empty_like(q_nope), qr=torch.empty_like(q_rope),
-                         h_out=torch.empty(dec_j.out.shape, dtype=dec_j.out.dtype).pin_memory()))
+        qn_j, qr_j = torch.empty_like(q_nope), torch.empty_like(q_rope)
+        sets.append(dict(dec=dec_j, ins=[qn_j, qr_j, lens_j] + ([bt_j] if bt_j is not None else []),
+                         out=dec_j.out, h_out=torch.empty(dec_j.out.shape, dtype=dec_j.out.dtype).pin_memory(),
+                         step=lambda dec_j=dec_j, qn_j=qn_j, qr_j=qr_j: dec_j.step(qn_j, qr_j)))
     e2e_steps = max(3, min(K, 50))
-    h2d = h_qn.numel() * 2 + h_qr.numel() * 2 + h_lens.numel() * 4 + (h_bt.numel() * 4 if h_bt is not None else 0)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sets[0]["h_out"].numel() * 2
-    copy = torch.cuda.Stream(dev)
-
-    def copy_in(j):
-        sj = sets[j]
-        with torch.cuda.stream(copy):
-            sj["qn"].copy_(h_qn, non_blocking=True)
-            sj["qr"].copy_(h_qr, non_blocking=True)
-            sj["lens"].copy_(h_lens, non_blocking=True)
-            if h_bt is not None:
-                sj["bt"].copy_(h_bt, non_blocking=True)
-            ev_in = torch.cuda.Event()
-            ev_in.record(copy)
-        return ev_in
-
-    def copy_out(j, ev_done):
-        with torch.cuda.stream(copy):
-            copy.wait_event(ev_done)
-            sets[j]["h_out"].copy_(sets[j]["dec"].out, non_blocking=True)
-
-    def e2e_loop(n):
-        """n pipelined steps on the current stream (compute) and the copy stream."""
-        cur = torch.cuda.current_stream(dev)
-        fork = torch.cuda.Event()
-        fork.record(cur)
-        copy.wait_event(fork)
-        ev_in = copy_in(0)
-        for i in range(n):
-            j = i % 2
-            cur.wait_event(ev_in)
-            sets[j]["dec"].step(sets[j]["qn"], sets[j]["qr"])
-            ev_done = torch.cuda.Event()
-            ev_done.record(cur)
-            if i + 1 < n:
-                ev_in = copy_in(1 - j)  # queued behind the read-back of step i-1, which used that set
-            copy_out(j, ev_done)
-        join = torch.cuda.Event()
-        join.record(copy)
-        cur.wait_event(join)
-
-    # The loop is captured once as a CUDA graph, so that the host's per-step launch
-    # work (four copies, the step, the events) does not pace the GPU; where capture
-    # is refused the same loop runs eagerly.
-    e2e_mode = "graph"
-    graph = torch.cuda.CUDAGraph()
-    try:
-        e2e_loop(2)  # warm the copy paths outside the capture
-        torch.cuda.synchronize(dev)
-        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
-            e2e_loop(e2e_steps)
-        graph.replay()
-        torch.cuda.synchronize(dev)
-    except RuntimeError:
-        torch.cuda.synchronize(dev)
-        e2e_mode = "eager"
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(active)
-    e0.record(stream)
-    if e2e_mode == "graph":
-        graph.replay()
-    else:
-        e2e_loop(e2e_steps)
-    e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active,
-                        "cuda" if active and args.backend == "nccl" else "cpu")
+    barrier(active)
+    e2e_local, e2e_mode = pipelined_e2e(dev, host_in, sets, e2e_steps)
+    e2e_ms = reduce_max(e2e_local, active, "cuda" if active and args.backend == "nccl" else "cpu")
     if any(mla.read_status(sj["dec"].workspace) != 0 for sj in sets):
         raise RuntimeError("device status after the end-to-end loop")
 
@@ -493,6 +433,71 @@ def _timed_steps(step, K, flush, stream, dev):
         ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     return [a.elapsed_time(b) for a, b in ev]
+
+
+def pipelined_e2e(dev, host_in, sets, n_steps):
+    """End-to-end time per step through the public API: step i copies host_in (pinned)
+    into its set's device inputs and reads its set's output back to pinned memory, on a
+    copy stream that overlaps the neighbouring steps' compute (two alternating sets, so
+    that a set is refilled only after its step ran and its result was read).  The loop
+    is captured once as a CUDA graph, so that the host's launch work does not pace the
+    GPU; where capture is refused the same loop runs eagerly.
+    sets: two dicts with "ins" (device tensors in host_in's order), "out" (device),
+    "h_out" (pinned host) and "step" (issues the step on the current stream).
+    Returns (ms per step, "graph" | "eager")."""
+    copy = torch.cuda.Stream(dev)
+
+    def copy_in(j):
+        with torch.cuda.stream(copy):
+            for dst, src in zip(sets[j]["ins"], host_in):
+                dst.copy_(src, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy)
+        return ev
+
+    def loop(n):
+        cur = torch.cuda.current_stream(dev)
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        copy.wait_event(fork)
+        ev_in = copy_in(0)
+        for i in range(n):
+            j = i % 2
+            cur.wait_event(ev_in)
+            sets[j]["step"]()
+            done = torch.cuda.Event()
+            done.record(cur)
+            if i + 1 < n:
+                ev_in = copy_in(1 - j)  # queued behind the read-back of step i-1, which used that set
+            with torch.cuda.stream(copy):
+                copy.wait_event(done)
+                sets[j]["h_out"].copy_(sets[j]["out"], non_blocking=True)
+        join = torch.cuda.Event()
+        join.record(copy)
+        cur.wait_event(join)
+
+    stream = torch.cuda.current_stream(dev)
+    mode = "graph"
+    graph = torch.cuda.CUDAGraph()
+    try:
+        loop(2)  # the copy paths, eagerly, before the capture
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            loop(n_steps)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    except RuntimeError:
+        torch.cuda.synchronize(dev)
+        mode = "eager"
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    if mode == "graph":
+        graph.replay()
+    else:
+        loop(n_steps)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / n_steps, mode
 
 
 TOPK = 2048  # DeepSeek-V3.2's index_topk
@@ -712,17 +717,20 @@ def main_prefill(args, cfg, rank, world, local, active):
     h_qn, h_qr = inp["q_nope"].pin_memory(), inp["q_rope"].pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
+    sets = []
+    for _ in range(2):
+        bufs = dict(qn=torch.empty_like(d["q_nope"]), qr=torch.empty_like(d["q_rope"]), out=torch.empty_like(out),
+                    lse=torch.empty_like(lse), ws=torch.empty_like(ws))
+
+        def prefill_step(b=bufs):
+            mla.prefill(prob, b["qn"], b["qr"], cache, d["w_uk"], d["w_uv"], out=b["out"], lse=b["lse"],
+                        workspace=b["ws"])
+        sets.append(dict(ins=[bufs["qn"], bufs["qr"]], out=bufs["out"],
+                         h_out=torch.empty(out.shape, dtype=out.dtype).pin_memory(), step=prefill_step))
+    del bufs
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        d["q_nope"].copy_(h_qn, non_blocking=True)
-        d["q_rope"].copy_(h_qr, non_blocking=True)
-        step()
-        h_out.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active, "cuda" if active and args.backend == "nccl" else "cpu")
+    e2e_local, e2e_mode = pipelined_e2e(dev, [h_qn, h_qr], sets, e2e_steps)
+    e2e_ms = reduce_max(e2e_local, active, "cuda" if active and args.backend == "nccl" else "cpu")
     if rank != 0:
         return
     pk = peaks()
@@ -768,7 +776,9 @@ def main_prefill(args, cfg, rank, world, local, active):
         "cpu_baseline": cpu,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": (h_qn.numel() + h_qr.numel()) * 2, "d2h_bytes_per_step": h_out.numel() * 2,
-                "note": "pinned host q_nope/q_rope in, out back, every step; cache and weights resident"},
+                "note": "pinned host q_nope/q_rope in, out back, every step, on a copy stream overlapping the "
+                        "neighbouring steps' compute (two alternating buffer sets); cache and weights resident",
+                "launch": e2e_mode},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
         "step_ms_min": min(step_ms),
@@ -884,18 +894,22 @@ def main_sparse(args, cfg, rank, world, local, active):
     h_qn, h_qr, h_idx = inp["q_nope"].pin_memory(), inp["q_rope"].pin_memory(), idx.pin_memory()
     h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e2e_steps = max(3, min(K, 50))
+    sets = []
+    for _ in range(2):
+        bufs = dict(qn=torch.empty_like(d["q_nope"]), qr=torch.empty_like(d["q_rope"]), idx=torch.empty_like(d_idx),
+                    q_cat=torch.empty_like(q_cat), o_lat=torch.empty_like(o_lat), lse=torch.empty_like(lse),
+                    out=torch.empty_like(out), ws=torch.empty_like(ws))
+
+        def sparse_step(b=bufs):
+            mla.absorb_q(prob, b["qn"], b["qr"], d["w_uk"], q_cat=b["q_cat"])
+            mla.decode_attn_sparse(prob, b["q_cat"], cache, b["idx"], num_splits=args.splits, o_lat=b["o_lat"],
+                                   lse=b["lse"], workspace=b["ws"])
+            mla.out_proj(prob, b["o_lat"], d["w_uv"], out=b["out"])
+        sets.append(dict(ins=[bufs["qn"], bufs["qr"], bufs["idx"]], out=bufs["out"],
+                         h_out=torch.empty(out.shape, dtype=out.dtype).pin_memory(), step=sparse_step))
     torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        d["q_nope"].copy_(h_qn, non_blocking=True)
-        d["q_rope"].copy_(h_qr, non_blocking=True)
-        d_idx.copy_(h_idx, non_blocking=True)
-        absorb(); attend(); project()
-        h_out.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, active, "cuda" if active and args.backend == "nccl" else "cpu")
+    e2e_local, e2e_mode = pipelined_e2e(dev, [h_qn, h_qr, h_idx], sets, e2e_steps)
+    e2e_ms = reduce_max(e2e_local, active, "cuda" if active and args.backend == "nccl" else "cpu")
     if rank != 0:
         return
     pk = peaks()
@@ -940,7 +954,9 @@ def main_sparse(args, cfg, rank, world, local, active):
         "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": (h_qn.numel() + h_qr.numel()) * 2 + h_idx.numel() * 4,
                 "d2h_bytes_per_step": h_out.numel() * 2,
-                "note": "pinned host q_nope/q_rope/index lists in, out back, every step; cache and weights resident"},
+                "note": "pinned host q_nope/q_rope/index lists in, out back, every step, on a copy stream "
+                        "overlapping the neighbouring steps' compute (two alternating buffer sets); cache and "
+                        "weights resident", "launch": e2e_mode},
         "gpu_launches": 3 * K,
         "clocks": clocks.summary(),
         "step_ms_min": min(step_ms),
