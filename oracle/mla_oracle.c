@@ -28,7 +28,7 @@
  *             key per token, shared by all heads; with an FP8 latent the same
  *             576 values take one byte each).
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *  - the cached token row is [c_kv (d_c) | k_rope (d_rope)], contiguous;
  *  - q_rope and k_rope arrive already rotated; no rotation happens here;
  *  - seq_lens[b] counts the s_q new tokens, already appended; query i
