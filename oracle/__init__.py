@@ -1,6 +1,6 @@
 """fp64 CPU oracle for weight-absorbed MLA decode -- TEST INFRASTRUCTURE.
 
-This package is the checker, not the product.  Only ``tests/``,
+This package is what the CUDA path is checked against, not the product.  Only ``tests/``,
 ``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
 ``bench.py`` may import it.  It shares no code with the CUDA library and never
 imports it; the two meet only through the seeded input generators, which hold

@@ -1,7 +1,7 @@
 /*
  * fp64 CPU oracle for weight-absorbed Multi-head Latent Attention (MLA) decode.
  *
- * TEST INFRASTRUCTURE ONLY.  This file is the checker, not the product: only the
+ * TEST INFRASTRUCTURE ONLY.  The CUDA path is checked against it; it is not the product: only the
  * test suite, the smoke check and the benchmark's CPU-baseline / reference legs
  * load it.  It shares no code, header, table or helper with the CUDA library.
  *
