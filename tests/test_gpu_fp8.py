@@ -118,6 +118,22 @@ def test_fp8_full_size_sampled():
     assert _check(cfg, _fp8_inputs(cfg), rows=sample_rows(cfg, 48)) == 0
 
 
+@pytest.mark.parametrize("paged", [False, True])
+def test_fp8_last_wave_tail(paged):
+    """80 work items on 76 cluster slots with an FP8 cache: the last sequence runs in
+    pieces merged by the tail combine (no longest-first order for FP8); its rows and
+    a sample of the others against the oracle."""
+    cfg = MLAConfig("fp8_tail", B=20, s_q=4, T=1024, paged=paged, seed=63, **_DSV3)
+    inp = _fp8_inputs(cfg)
+    d = to_dev(inp)
+    prob = mla.Problem.of(cfg)
+    cache = mla.make_cache(prob, d["kv"], d["seq_lens"], d["block_table"], cfg.page_size, kv_scale=KV_FP8_SCALE)
+    assert mla.decode_num_splits(prob, cache) == 2
+    rows = cfg.s_q * cfg.H
+    tail = list(range((cfg.B - 1) * rows, cfg.B * rows, 29))
+    assert _check(cfg, inp, rows=sorted(set(sample_rows(cfg, 16) + tail)), end_to_end=True) == 0
+
+
 def test_fp8_rejected_where_unsupported():
     cfg = MLAConfig("fp8_bad", B=2, H=16, d_c=64, d_rope=16, d_nope=32, d_v=32, s_q=1, T=128, seed=48)
     inp = to_dev(_fp8_inputs(cfg))
