@@ -19,6 +19,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -127,12 +128,18 @@ ATTN_SOURCES = ("api.cu", "attn_tc.cu", "combine.cu", "common.cuh", "launch.h", 
 
 
 def source_hash() -> str:
+    """Hash of the attention's sources with comments and blank space taken out (an
+    edited comment leaves the kernel as it was)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_decode_attention_absorbed_gb300", "csrc")
     for name in ATTN_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", "", text)                  # line comments
+        text = "\n".join(line.strip() for line in text.splitlines() if line.strip())
+        h.update(name.encode())
+        h.update(text.encode())
     return h.hexdigest()
 
 

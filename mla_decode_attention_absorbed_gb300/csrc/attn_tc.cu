@@ -56,6 +56,15 @@
 // warps 12-15: converters (FP8) or loaders (bf16 sparse).
 // Every wait is bounded; a lost wait records MLA_ERR_TIMEOUT, drains what is in
 // flight, and the CTA returns.
+//
+// Work order (grid z): item z is sequence z, piece blockIdx.y of num_splits; with
+// a tail (tail_splits > 1) items past tail_b0 are the pieces of the last
+// sequences, so that they fill the last wave; with the longest-first order (dense
+// bf16) item positions map to sequences by rank of length, every CTA ranking
+// the lengths itself.  Around the tile loop: the producer holds the ring after
+// the first tile until the queries are in (no preceding grid), the queries load
+// coalesced and turn row-per-lane through shared memory, and O leaves through a
+// shared-memory copy as whole-row stores.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
