@@ -46,7 +46,9 @@
  *  - Dimensions: H >= 1, s_q >= 1, d_c a multiple of 64 up to 512, d_rope a
  *    multiple of 16 up to 64, d_nope and d_v multiples of 16 from 16 to 256,
  *    s_q * H <= 65536 (the prefill entry points: s_q <= 2^20 on the expand
- *    path).  Other shapes return MLA_ERR_UNSUPPORTED.
+ *    path), B and H at most 65535, B * s_q at most 65535 * 128, and on the
+ *    expand path B * H at most 65535 (launch grid limits).  Other shapes return
+ *    MLA_ERR_UNSUPPORTED.
  */
 #ifndef MLA_H
 #define MLA_H

@@ -14,6 +14,7 @@ constexpr int kMaxSplits = 64;
 constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (split planning only)
 constexpr size_t kStatusBytes = 256;  // status word + padding at the workspace start
 constexpr int kMaxOrdered = 1024;     // longest-first work order up to this many sequences
+constexpr int kMaxGridZ = 65535;      // largest third grid dimension of a launch
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -29,6 +30,10 @@ int check_shape(const mla_dims *d) {
     if (d->d_nope % 16 || d->d_nope > 256) return MLA_ERR_UNSUPPORTED;
     if (d->d_v % 16 || d->d_v > 256) return MLA_ERR_UNSUPPORTED;
     if (d->s_q > (1 << 20)) return MLA_ERR_UNSUPPORTED;
+    // grid limits: heads index the projections' third grid dimension, sequences
+    // the attention's (65535 at most in either)
+    if (d->H > kMaxGridZ || d->B > kMaxGridZ) return MLA_ERR_UNSUPPORTED;
+    if ((long long)d->B * d->s_q > (long long)kMaxGridZ * 128) return MLA_ERR_UNSUPPORTED;  // 128-token GEMM tiles
     if (!(d->scale == d->scale)) return MLA_ERR_SHAPE;  // NaN scale
     return MLA_OK;
 }
@@ -120,6 +125,7 @@ long long expanded_width(const mla_dims *d) { return (long long)d->d_v + d->d_no
 int check_expand(const mla_dims *d, const mla_cache *c) {
     if (c->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
     if (d->d_v % 64 || d->d_nope % 64 || d->d_v + d->d_nope > 256 || expanded_width(d) > 320) return MLA_ERR_UNSUPPORTED;
+    if ((long long)d->B * d->H > kMaxGridZ) return MLA_ERR_UNSUPPORTED;  // one work item per (sequence, head)
     return MLA_OK;
 }
 
@@ -168,7 +174,7 @@ DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
     const long long cap = ((maxL + 63) / 64) / 8;  // pieces of at least 8 tiles
     if (k > cap) k = cap;
     if (k > kMaxSplits) k = kMaxSplits;
-    if (k < 2) return pl;
+    if (k < 2 || d->B - b_tail + b_tail * k > kMaxGridZ) return pl;
     pl.b_tail = (int)b_tail;
     pl.tail_splits = (int)k;
     return pl;

@@ -65,7 +65,8 @@ def test_host_validation_without_gpu(lib):
     # misaligned pointer
     assert lib.mla_absorb_q(ctypes.byref(d), ctypes.c_void_p(0x40008), a, a, a, nul) == 4
     # unsupported shapes
-    for bad in (dict(d_c=96), dict(d_c=1024), dict(d_rope=8), dict(d_nope=24), dict(d_v=512), dict(H=65537)):
+    for bad in (dict(d_c=96), dict(d_c=1024), dict(d_rope=8), dict(d_nope=24), dict(d_v=512), dict(H=65537),
+                dict(H=65536), dict(B=65536), dict(B=65535, s_q=129)):
         p = dsv3()
         for k, v in bad.items():
             setattr(p, k, v)
@@ -124,6 +125,20 @@ def test_tail_plan_fills_the_last_wave(lib):
     # pieces stay at least 8 tiles long: a 1024-token history allows 2 pieces
     d = dsv3(B=20, s_q=4).dims()  # 80 work items: one sequence in the last wave
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(fake_cache(1024))) == 2
+
+
+def test_expand_path_grid_limit(lib):
+    """The expanded prefill runs one work item per (sequence, head): past 65535 of
+    them it is unsupported, and the dispatch sizes the absorbed form instead."""
+    nul = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(0x40000)
+    c = fake_cache(4096)
+    ok = dsv3(B=511, s_q=256).dims()  # 511 x 128 = 65,408 work items
+    big = dsv3(B=512, s_q=256).dims()  # 65,536
+    assert lib.mla_prefill_expand_workspace_size(ctypes.byref(ok), ctypes.byref(c)) > 0
+    assert lib.mla_prefill_expand_workspace_size(ctypes.byref(big), ctypes.byref(c)) == 0
+    assert lib.mla_prefill_expand(ctypes.byref(big), a, a, ctypes.byref(c), a, a, a, a, a, 1 << 40, nul) == 6
+    assert lib.mla_prefill_workspace_size(ctypes.byref(big), ctypes.byref(c)) > 0  # the absorbed form
 
 
 def test_prefill_crossover_matches_the_pages_formula(lib):
