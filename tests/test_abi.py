@@ -125,6 +125,11 @@ def test_tail_plan_fills_the_last_wave(lib):
     # pieces stay at least 8 tiles long: a 1024-token history allows 2 pieces
     d = dsv3(B=20, s_q=4).dims()  # 80 work items: one sequence in the last wave
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(fake_cache(1024))) == 2
+    # the tail's pieces must still fit the grid: 65,535 sequences leave no room for them
+    d = dsv3(B=65535, s_q=1).dims()  # 65,535 items = 862 waves + 23
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
+    d = dsv3(B=65535 - 76, s_q=1).dims()  # 65,459 items = 861 waves + 23: 23 x 3 pieces fit
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 3
 
 
 def test_expand_path_grid_limit(lib):
