@@ -192,7 +192,22 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "nvidia-smi every 100 ms over 1 s of the same steps untimed, "
+                                              "then the timed steps"}
+
+
+def soak(step, dev, seconds=1.0, flush=None):
+    """Runs the step, untimed, for about `seconds` right before the timed region, so
+    that the clock samples (every 100 ms) see the clocks under this very load and
+    the timed steps start from a warm, sustained state."""
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(20):
+            if flush is not None:
+                flush.zero_()
+            step()
+        torch.cuda.synchronize(dev)
 
 
 # ------------------------------------------------------------------------- our arm
@@ -258,7 +273,7 @@ def run_ours(cfg, args, rank, world, local, active):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(local).start()
-    time.sleep(0.3)
+    soak(step, dev, 1.0, flush)
     barrier(active)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
@@ -578,7 +593,7 @@ def main_op(args):
         step()
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(local).start()
-    time.sleep(0.3)
+    soak(graph.replay, dev, 1.0, flush)
     barrier(active)
     step_ms = _timed_steps(graph.replay, args.steps, flush, stream, dev)
     barrier(active)
@@ -713,7 +728,7 @@ def main_prefill(args, cfg, rank, world, local, active):
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
     clocks = ClockSampler(local).start()
-    time.sleep(0.3)
+    soak(step, dev, 1.0, flush)
     barrier(active)
     step_ms = _timed_steps(step, args.steps, flush, stream, dev)
     barrier(active)
@@ -888,7 +903,7 @@ def main_sparse(args, cfg, rank, world, local, active):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(local).start()
-    time.sleep(0.3)
+    soak(lambda: (absorb(), attend(), project()), dev, 1.0, flush)
     barrier(active)
     torch.cuda.synchronize(dev)
     for k in range(K):
