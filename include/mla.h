@@ -240,8 +240,10 @@ MLA_API int mla_cache_append(const mla_dims *dims, int d_model, const void *x, c
                              void *stream);
 
 /* Bytes of workspace mla_naive_decode needs: the materialised per-head K and V
- * of every visible cached token (B*H*capacity*(d_nope+d_v) bf16) plus the
- * status word.  Returns 0 for invalid arguments. */
+ * of every cached token plus the status word (with the tensor-core expansion,
+ * rows [V_h | K_h | k_rope] of B*H*capacity*(d_v+d_nope+d_rope) bf16 and the
+ * concatenated queries; otherwise B*H*capacity*(d_nope+d_v) bf16).  Returns 0
+ * for invalid arguments, or when B*H exceeds 65535. */
 MLA_API size_t mla_naive_workspace_size(const mla_dims *dims, const mla_cache *cache);
 
 /* Decompress-then-attend, the comparison path ("The MLA decode speedup hiding
@@ -250,7 +252,12 @@ MLA_API size_t mla_naive_workspace_size(const mla_dims *dims, const mla_cache *c
  * and every cached token, K = c_kv . W_UK[h] and V = c_kv . W_UV[h] are written
  * to the workspace, then standard attention runs with the RoPE key appended:
  *   s_j = scale * (q_nope . K_j + q_rope . k_rope_j),  out = sum_j softmax(s)_j V_j.
- * Same tensors as the absorbed path; out [B][s_q][H][d_v] bf16, lse fp32 [B][s_q][H]. */
+ * Same tensors as the absorbed path; out [B][s_q][H][d_v] bf16, lse fp32 [B][s_q][H].
+ * Where the prefill expansion takes the shape (bf16 cache, d_v and d_nope multiples
+ * of 64, d_v + d_nope <= 256, d_v + d_nope + d_rope <= 320) the decompression is
+ * that tcgen05 GEMM and the attention runs per head on the tensor cores, the same
+ * launches as mla_prefill_expand; other shapes use CUDA-core kernels.  B*H above
+ * 65535 (one grid slice per sequence and head) returns MLA_ERR_UNSUPPORTED. */
 MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const void *q_rope,
                              const mla_cache *cache, const void *w_uk, const void *w_uv,
                              void *out, float *lse, void *workspace, size_t ws_bytes,
@@ -267,11 +274,11 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
  * compiled into the library (a file-scope __device__ array; every GPU on which
  * the library's kernels are loaded holds it until the process exits).  Nothing
  * is allocated or freed by this call.
- *  - The first call on each device looks the array's device address up once
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
- *  - num_splits 0 takes the library's split count if its partials fit in the
- *    array, else the largest count that fits (1 always fits).  An explicit
+ *  - Every call looks the array's device address up (cudaGetSymbolAddress,
+ *    with the device current); the first call on a device loads the library's
+ *    module there, so make that first call before any stream capture.
+ *  - num_splits 0 takes the library's split count (its partials stay near one
+ *    wave of work items, about 20 MB, within the array); an explicit
  *    num_splits whose partials exceed 32 MiB returns MLA_ERR_WORKSPACE.
  *  - Every call shares the one array and overwrites it: calls that overlap on
  *    the GPU (other streams, other host threads, without ordering between them)

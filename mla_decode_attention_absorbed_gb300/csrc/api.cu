@@ -11,7 +11,17 @@ namespace {
 
 constexpr int kAbiVersion = 2;
 constexpr int kMaxSplits = 64;
-constexpr int kNumSMs = 152;          // GB300: 2 dies x 76 SMs (split planning only)
+// SMs of the current device (split planning only), looked up once per device
+int num_sms() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+    if (dev < 64 && cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 2) n = 152;
+    if (dev < 64) cached[dev] = n;
+    return n;
+}
 constexpr size_t kStatusBytes = 256;  // status word + padding at the workspace start
 constexpr int kMaxOrdered = 1024;     // longest-first work order up to this many sequences
 constexpr int kMaxGridZ = 65535;      // largest third grid dimension of a launch
@@ -88,7 +98,7 @@ int plan_splits_len(const mla_dims *d, long long maxL, int requested) {
     // the history only while the pieces still fit in one wave of the GPU (more
     // pieces would add a partial wave and the cross-split merge), and keep every
     // piece at least 8 tiles long.
-    const long long slots = d->d_c > 256 ? kNumSMs / 2 : kNumSMs;
+    const long long slots = d->d_c > 256 ? num_sms() / 2 : num_sms();
     long long want = slots / units;
     long long cap = tiles / 8;
     if (want > cap) want = cap;
@@ -163,7 +173,7 @@ DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
     DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1, false};
     const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
     const long long units = (long long)d->B * row_blocks;
-    const long long slots = d->d_c > 256 ? kNumSMs / 2 : kNumSMs;
+    const long long slots = d->d_c > 256 ? num_sms() / 2 : num_sms();
     pl.lpt = pl.splits == 1 && units > slots && d->B <= kMaxOrdered && c->kv_dtype == MLA_KV_BF16;
     if (requested > 0 || pl.splits > 1) return pl;
     const long long rem = units % slots;
@@ -248,6 +258,48 @@ mla::AttnParams make_params(const mla_dims *d, const mla_cache *c) {
     p.max_pages = c->max_pages; p.page_size = c->page_size; p.num_pages = c->num_pages;
     p.seq_lens = c->seq_lens;
     return p;
+}
+
+// The expand form ("Why MLA and MTP Fight Each Other", 5.3/5.5: materialise K_h,
+// V_h, then attend per head): expansion GEMM into the workspace, query concat,
+// per-head attention.  Arguments already checked; the status word is reset.
+int run_expand(const mla_dims *dims, const void *q_nope, const void *q_rope, const mla_cache *cache,
+               const void *w_uk, const void *w_uv, void *out, float *lse, void *workspace, cudaStream_t st) {
+    char *base = (char *)workspace + kStatusBytes;
+    void *q_exp = base;
+    void *expd = base + expand_q_bytes(dims);
+    mla::AttnParams p = make_params(dims, cache);
+    p.status = (int *)workspace;
+    cudaError_t e = mla::launch_expand_kv(p, dims->d_nope, dims->d_v, w_uk, w_uv, expd, st);
+    if (e == cudaSuccess) e = mla::launch_concat_q(*dims, q_nope, q_rope, q_exp, st);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    // per-head attention: (sequence, head) pairs over the expanded rows
+    mla::AttnParams a = p;
+    a.B = dims->B * dims->H;
+    a.H = 1;
+    a.d_c = dims->d_v;
+    a.d_rope = dims->d_nope + dims->d_rope;
+    a.kv = expd;
+    a.block_table = nullptr;
+    a.capacity = (int)cache_capacity(cache);
+    a.seq_stride = (long long)a.capacity * expanded_width(dims);
+    a.q_cat = (const __nv_bfloat16 *)q_exp;
+    a.q_w = dims->d_nope + dims->d_rope;
+    a.heads_per_seq = dims->H;
+    a.o_lat = (__nv_bfloat16 *)out;
+    a.lse = lse;
+    a.num_splits = 1;
+    e = mla::launch_attn_expand(a, st);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// The naive comparison path runs on the tensor cores (the expand form) where
+// those kernels take the shape, else on the CUDA-core kernels of naive.cu.
+bool naive_on_expand(const mla_dims *d, const mla_cache *c) { return check_expand(d, c) == MLA_OK; }
+
+size_t naive_cuda_core_bytes(const mla_dims *d, const mla_cache *c) {
+    size_t per = (size_t)d->B * d->H * (size_t)cache_capacity(c);
+    return kStatusBytes + round_up(per * d->d_nope * 2, 256) + per * d->d_v * 2;
 }
 
 }  // namespace
@@ -413,8 +465,8 @@ MLA_API int mla_out_proj(const mla_dims *dims, const void *o_lat, const void *w_
 
 MLA_API size_t mla_naive_workspace_size(const mla_dims *dims, const mla_cache *cache) {
     if (check_dims(dims) || check_cache(dims, cache)) return 0;
-    size_t per = (size_t)dims->B * dims->H * (size_t)cache_capacity(cache);
-    return kStatusBytes + round_up(per * dims->d_nope * 2, 256) + per * dims->d_v * 2;
+    if ((long long)dims->B * dims->H > kMaxGridZ) return 0;  // one (sequence, head) per grid slice
+    return naive_on_expand(dims, cache) ? expand_workspace_bytes(dims, cache) : naive_cuda_core_bytes(dims, cache);
 }
 
 MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const void *q_rope,
@@ -425,6 +477,7 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
     if (!cache) return MLA_ERR_NULL;
     if ((s = check_cache(dims, cache))) return s;
     if (cache->kv_dtype != MLA_KV_BF16) return MLA_ERR_UNSUPPORTED;
+    if ((long long)dims->B * dims->H > kMaxGridZ) return MLA_ERR_UNSUPPORTED;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     if (ws_bytes < mla_naive_workspace_size(dims, cache)) return MLA_ERR_WORKSPACE;
@@ -437,6 +490,7 @@ MLA_API int mla_naive_decode(const mla_dims *dims, const void *q_nope, const voi
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
     if (dims->B == 0) return MLA_OK;
+    if (naive_on_expand(dims, cache)) return run_expand(dims, q_nope, q_rope, cache, w_uk, w_uv, out, lse, workspace, st);
     mla::AttnParams p = make_params(dims, cache);
     p.status = (int *)workspace;
     char *kbuf = (char *)workspace + kStatusBytes;
@@ -480,32 +534,7 @@ MLA_API int mla_prefill_expand(const mla_dims *dims, const void *q_nope, const v
     cudaStream_t st = as_stream(stream);
     if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
     if (dims->B == 0) return MLA_OK;
-    char *base = (char *)workspace + kStatusBytes;
-    void *q_exp = base;
-    void *expd = base + expand_q_bytes(dims);
-    mla::AttnParams p = make_params(dims, cache);
-    p.status = (int *)workspace;
-    cudaError_t e = mla::launch_expand_kv(p, dims->d_nope, dims->d_v, w_uk, w_uv, expd, st);
-    if (e == cudaSuccess) e = mla::launch_concat_q(*dims, q_nope, q_rope, q_exp, st);
-    if (e != cudaSuccess) return MLA_ERR_CUDA;
-    // per-head attention: (sequence, head) pairs over the expanded rows
-    mla::AttnParams a = p;
-    a.B = dims->B * dims->H;
-    a.H = 1;
-    a.d_c = dims->d_v;
-    a.d_rope = dims->d_nope + dims->d_rope;
-    a.kv = expd;
-    a.block_table = nullptr;
-    a.capacity = (int)cache_capacity(cache);
-    a.seq_stride = (long long)a.capacity * expanded_width(dims);
-    a.q_cat = (const __nv_bfloat16 *)q_exp;
-    a.q_w = dims->d_nope + dims->d_rope;
-    a.heads_per_seq = dims->H;
-    a.o_lat = (__nv_bfloat16 *)out;
-    a.lse = lse;
-    a.num_splits = 1;
-    e = mla::launch_attn_expand(a, st);
-    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    return run_expand(dims, q_nope, q_rope, cache, w_uk, w_uv, out, lse, workspace, st);
 }
 
 MLA_API size_t mla_prefill_workspace_size(const mla_dims *dims, const mla_cache *cache) {

@@ -67,6 +67,7 @@
 // shared-memory copy as whole-row stores.
 #include <cuda_fp16.h>
 
+#include "attn_common.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "sm100.cuh"
@@ -76,6 +77,7 @@ namespace mla {
 namespace {
 
 using namespace sm100;
+using namespace attn;
 
 constexpr int kRows = 128;        // query rows per work item (MMA M)
 constexpr int kTile = 64;         // tokens per tile (MMA N of the score, K of the sum)
@@ -114,10 +116,6 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // gives up).  Each warpgroup runs its instruction once, on entering its roles.
 constexpr int kRegSoftmax = 136, kRegOther = 120;
 static_assert(2 * 128 * kRegSoftmax + 2 * 128 * kRegOther == 65536, "register split must equal the launch's total");
-template <int kRegs>
-__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs)); }
-template <int kRegs>
-__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs)); }
 
 constexpr uint32_t kColO = 0, kColS = 256, kColP = 320, kColQ = 352;
 constexpr float kRescaleLog2 = 8.0f;  // keep a stale maximum until scores exceed it by 2^8
@@ -160,45 +158,6 @@ struct Smem {
     int received; // last tile the softmax warps received
 };
 
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// Bounded wait that also gives up once the CTA is aborting.
-template <bool kCluster = false, class S>
-__device__ __forceinline__ bool wait_bar(S &sm, uint64_t *bar, uint32_t parity) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    const long long c0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (*(volatile int *)&sm.abort) return false;
-            if (wait_expired(t0, c0)) return false;
-        }
-    }
-}
-
-// Every lane waits; the warp proceeds only if all lanes saw the phase complete,
-// so warp-collective tcgen05 instructions that follow stay converged.
-template <bool kCluster = false, class S>
-__device__ __forceinline__ bool warp_wait(S &sm, uint64_t *bar, uint32_t parity) {
-    const bool ok = wait_bar<kCluster>(sm, bar, parity);
-    return __all_sync(0xffffffffu, ok);
-}
-
-template <bool kSplit, class S>
-__device__ __forceinline__ void raise_abort(S &sm, const AttnParams &p, uint32_t peer) {
-    *(volatile int *)&sm.abort = 1;
-    set_status(p.status, MLA_ERR_TIMEOUT);
-    if (kSplit) {
-        uint32_t remote = map_to_rank(smem_u32(&sm.abort), peer);
-        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(1) : "memory");
-    }
-}
-
 // This thread's 32 scores of the tile in S (tensor memory).
 __device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[kHalf]) {
     uint32_t u0[16], u1[16];
@@ -210,19 +169,6 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[kHalf]) {
         s[e] = __uint_as_float(u0[e]);
         s[16 + e] = __uint_as_float(u1[e]);
     }
-}
-
-// Two scores to fp16 (lo in the low half), saturating at +-65504 instead of
-// overflowing to infinity.
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    uint32_t d;
-    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
-    __half2 h = *reinterpret_cast<__half2 *>(&u);
-    return __half22float2(h);
 }
 
 // Four E4M3 codes (the bytes of u, lowest first) as four fp16 values (two
@@ -958,9 +904,9 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float2 theirs = unpack_f16x2(w4[e]);
-                        x[8 * c + 2 * e] = sc[8 * c + 2 * e] + theirs.x;
-                        x[8 * c + 2 * e + 1] = sc[8 * c + 2 * e + 1] + theirs.y;
+                        x[8 * c + 2 * e] = sc[8 * c + 2 * e];
+                        x[8 * c + 2 * e + 1] = sc[8 * c + 2 * e + 1];
+                        add_f16x2_to(w4[e], x[8 * c + 2 * e], x[8 * c + 2 * e + 1]);
                     }
                 }
                 if (more) stage(n + 1, sn);

@@ -7,8 +7,6 @@
 // synchronise the whole device) is not allowed while decoding.  For them the
 // split partials and the status word live in one fixed array compiled into
 // this library instead of a caller-provided workspace.
-#include <mutex>
-
 #include "common.cuh"
 
 namespace {
@@ -16,7 +14,6 @@ namespace {
 // Scratch of the no-allocation entry point.  Every GPU on which this library's
 // kernels are loaded holds these bytes until the process exits.
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
-constexpr int kMaxDevices = 64;
 
 }  // namespace
 
@@ -24,23 +21,15 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBy
 
 namespace {
 
-std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
-
 // Device address of g_decode_scratch on the current device.  In host code the
-// symbol's name only stands for it; the address comes from cudaGetSymbolAddress,
-// looked up once per device (with that device current) and then cached.
+// symbol's name only stands for it; the address comes from cudaGetSymbolAddress
+// with the device current.  It is looked up on every call (cheap once the
+// library's module is loaded on the device), so a reset device or a recreated
+// context, where the module and its array are loaded anew, gets the new address.
 int static_scratch(void **out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return MLA_ERR_CUDA;
+    *out = p;
     return MLA_OK;
 }
 
@@ -53,21 +42,15 @@ MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, con
     if (!dims || !cache) return MLA_ERR_NULL;
     if (num_splits < 0) return MLA_ERR_SHAPE;
     if (device_status && ((uintptr_t)device_status & 3u)) return MLA_ERR_ALIGN;
-    int splits = num_splits;
-    if (splits == 0 && mla_decode_workspace_size(dims, cache, 0) > kStaticScratchBytes) {
-        // The library's own plan when its partials fit, else the largest uniform count that fits.
-        splits = mla_decode_num_splits(dims, cache);
-        if (splits == 0) {  // the checks below report why the arguments are invalid
-            splits = 1;
-        }
-        while (splits > 1 && mla_decode_workspace_size(dims, cache, splits) > kStaticScratchBytes) --splits;
-    }
-    size_t need = mla_decode_workspace_size(dims, cache, splits);
+    // The library's plan keeps its split partials to about one wave of work items
+    // (about 20 MB at most), so it fits the array; a plan or an explicit split
+    // count that does not is refused.
+    const size_t need = mla_decode_workspace_size(dims, cache, num_splits);
     if (need > kStaticScratchBytes) return MLA_ERR_WORKSPACE;
     void *scratch = nullptr;
     int s = static_scratch(&scratch);
     if (s != MLA_OK) return s;
-    s = mla_decode_attn(dims, q_cat, cache, o_lat, lse, scratch, kStaticScratchBytes, splits, stream);
+    s = mla_decode_attn(dims, q_cat, cache, o_lat, lse, scratch, kStaticScratchBytes, num_splits, stream);
     if (s != MLA_OK) return s;
     if (device_status &&
         cudaMemcpyAsync(device_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice,

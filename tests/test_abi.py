@@ -155,3 +155,44 @@ def test_prefill_crossover_matches_the_pages_formula(lib):
         assert abs(mla.prefill_crossover(prob, L) - counts.crossover_S(512, 128, 128, L)) < 1e-9
     assert 127.5 < mla.prefill_crossover(prob, 512) < 128.5
     assert mla.prefill_crossover(prob, 0) == 0.0
+
+
+def test_naive_path_grid_limit(lib):
+    """The naive path runs one grid slice per (sequence, head): past 65535 of them
+    it is an argument error on the host, never a failed launch."""
+    nul = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(0x40000)
+    c = fake_cache(256)
+    ok = dsv3(B=511).dims()  # 511 x 128 = 65,408
+    big = dsv3(B=513).dims()  # 65,664
+    assert lib.mla_naive_workspace_size(ctypes.byref(ok), ctypes.byref(c)) > 0
+    assert lib.mla_naive_workspace_size(ctypes.byref(big), ctypes.byref(c)) == 0
+    assert lib.mla_naive_decode(ctypes.byref(big), a, a, ctypes.byref(c), a, a, a, a, a, 1 << 40, nul) == 6
+    # at DeepSeek-V3 widths the expansion holds rows [V_h | K_h | k_rope] (320 bf16)
+    d = dsv3(B=64).dims()
+    assert lib.mla_naive_workspace_size(ctypes.byref(d), ctypes.byref(fake_cache(4096))) >= 64 * 128 * 4096 * 320 * 2
+
+
+NOALLOC_BYTES = 32 << 20  # the no-allocation entry point's array
+
+
+def test_library_plan_fits_the_noalloc_array(lib):
+    """mla_decode_attn_noalloc runs the library's own plan (num_splits 0) in a fixed
+    32 MiB array: over the supported envelope that plan's workspace never exceeds it
+    (split partials stay near one wave of 128-row work items)."""
+    worst = 0
+    for d_c, d_rope in ((64, 16), (256, 64), (320, 16), (512, 64)):
+        for H, s_q in ((16, 1), (128, 1), (128, 2), (128, 4), (64, 3), (1, 1), (512, 128)):
+            for B in (1, 2, 3, 7, 20, 64, 65, 100, 151, 1000, 20000):
+                for T in (64, 1000, 4096, 32768, 1 << 20):
+                    if s_q > T or B * s_q > 65535 * 128:
+                        continue
+                    p = mla.Problem(B, H, s_q, d_c, d_rope, 128, 128, 0.1)
+                    d = p.dims()
+                    for paged in (False, True):
+                        c = fake_cache(T, paged)
+                        if not paged:
+                            c = mla.Cache(0x10000, T * (d_c + d_rope), T, None, 0, 64, 0, 0x20000, 0)
+                        n = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 0)
+                        worst = max(worst, n)
+    assert 0 < worst <= NOALLOC_BYTES, worst

@@ -46,6 +46,14 @@ CASES = [
                              len_hi=300, seed=7), 2),
     ("mid_dims", MLAConfig("md", B=2, H=40, d_c=192, d_rope=32, d_nope=64, d_v=48, s_q=2, len_lo=70,
                            len_hi=260, seed=8), 0),
+    # pair kernel shapes other than DeepSeek-V3's: a partial RoPE box (d_rope 48), two query
+    # tokens per 128-row block (H 64), a CTA whose second score chain is empty (d_c 320, d_rope 16)
+    ("pair_dc384_rope48", MLAConfig("q1", B=2, H=64, d_c=384, d_rope=48, d_nope=64, d_v=64, s_q=2, len_lo=70,
+                                    len_hi=400, seed=21), 0),
+    ("pair_dc320_rope16", MLAConfig("q2", B=3, H=128, d_c=320, d_rope=16, d_nope=64, d_v=64, s_q=1, len_lo=1,
+                                    len_hi=300, paged=True, seed=22), 2),
+    ("pair_dc448_rope32", MLAConfig("q3", B=2, H=128, d_c=448, d_rope=32, d_nope=128, d_v=128, s_q=3, len_lo=3,
+                                    len_hi=260, seed=23), 0),
 ]
 
 
