@@ -124,7 +124,7 @@ def traffic_for(kernel_key: str):
 # headers it includes, the merge, and the entry points that choose grid and plan.
 # A change elsewhere (the projections, the expansion, the naive path) leaves the
 # attention kernel, and so its captured DRAM traffic, as it was.
-ATTN_SOURCES = ("api.cu", "attn_tc.cu", "combine.cu", "common.cuh", "launch.h", "sm100.cuh", "tmap.h")
+ATTN_SOURCES = ("api.cu", "attn_common.cuh", "attn_tc.cu", "combine.cu", "common.cuh", "launch.h", "sm100.cuh", "tmap.h")
 
 
 def source_hash() -> str:
@@ -144,20 +144,38 @@ def source_hash() -> str:
 
 
 # ------------------------------------------------------------------------- clocks
+def nvsmi_gpu_id(local: int) -> str:
+    """The id nvidia-smi should sample for CUDA device `local`: its UUID (else its
+    PCI bus id).  nvidia-smi numbers GPUs its own way and ignores
+    CUDA_VISIBLE_DEVICES, so an ordinal could name another user's GPU."""
+    try:
+        props = torch.cuda.get_device_properties(local)
+        u = str(getattr(props, "uuid", "") or "")
+        u = u[4:] if u.startswith("GPU-") else u
+        if re.fullmatch(r"[0-9a-fA-F]{8}(-[0-9a-fA-F]{4}){3}-[0-9a-fA-F]{12}", u):
+            return "GPU-" + u
+        bus, devid = getattr(props, "pci_bus_id", None), getattr(props, "pci_device_id", None)
+        if bus is not None and devid is not None:  # a UUID the process may not see in full
+            return f"{getattr(props, 'pci_domain_id', 0):08x}:{bus:02x}:{devid:02x}.0"
+    except Exception:  # noqa: BLE001 - no device properties: fall back to the ordinal
+        pass
+    return str(local)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_id: str):
         self.proc = None
-        self.gpu = gpu_index
+        self.gpu = gpu_id
         self.lines = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -190,10 +208,10 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "gpu": self.gpu}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "window": "nvidia-smi every 100 ms over 1 s of the same steps untimed, "
-                                              "then the timed steps"}
+                "samples": len(sm), "gpu": self.gpu,
+                "window": "nvidia-smi every 100 ms over 1 s of the same steps untimed, then the timed steps"}
 
 
 def soak(step, dev, seconds=1.0, flush=None):
@@ -210,99 +228,215 @@ def soak(step, dev, seconds=1.0, flush=None):
         torch.cuda.synchronize(dev)
 
 
+def capture(fn, dev):
+    """fn's launches captured once as a CUDA graph (its host-side argument checks and
+    tensor-map encoding done at capture), returned as a replay callable; None where
+    capture is refused."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            fn()
+        g.replay()
+        torch.cuda.synchronize(dev)
+    except RuntimeError:
+        torch.cuda.synchronize(dev)
+        return None
+    return g.replay
+
+
+def roofline_of(w, attn_ms, pk):
+    """The attention kernel against the slower of its FLOPs at the bf16 peak and its
+    bytes at the HBM copy bandwidth (both measured)."""
+    attn_s = attn_ms * 1e-3
+    tensor_bound = w["attn_flops"] / (pk["bf16_tflops"] * 1e12) > w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        achieved = w["attn_flops"] / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_tflops"]}
+    else:
+        achieved = w["attn_bytes"] / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"]}
+    roof["peak_source"] = pk["source"] + (" burst bf16" if tensor_bound else " HBM copy")
+    roof["roofline_time_us"] = max(w["attn_flops"] / (pk["bf16_tflops"] * 1e12),
+                                   w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)) * 1e6
+    roof["kernel_us"] = attn_ms * 1e3
+    return roof
+
+
 # ------------------------------------------------------------------------- our arm
+class DecodeRun:
+    """One decode workload on this rank's GPU: inputs, a Decoder, and the decode
+    step and the attention alone each captured as a CUDA graph."""
+
+    def __init__(self, cfg, args, rank, dev, kv="bf16"):
+        from mla_decode_attention_absorbed_gb300 import mla
+        self.c = c = cfg.with_(seed=replica_seed(cfg.seed, rank))
+        self.inp = inp = make_inputs(c)
+        self.kv_scale = None
+        if kv == "fp8":
+            inp["kv"] = to_fp8_cache(inp["kv"])
+            self.kv_scale = inp["kv_scale"] = KV_FP8_SCALE
+        self.w = work(c, inp["seq_lens"].tolist(), 1 if kv == "fp8" else 2)
+        self.d = d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        self.prob = prob = mla.Problem.of(c)
+        self.dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], c.page_size,
+                               max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=self.kv_scale)
+        self.splits = mla.decode_num_splits(prob, self.dec.cache) if args.splits == 0 else args.splits
+        self.dev = dev
+        self.eager_step = lambda: self.dec.step(d["q_nope"], d["q_rope"])
+        self.eager_attend = lambda: self.dec.attend()
+        self.step = self.attend = None
+
+    def warm(self, warmup, flush):
+        from mla_decode_attention_absorbed_gb300 import mla
+        for _ in range(warmup):
+            if flush is not None:
+                flush.zero_()
+            self.eager_step()
+        torch.cuda.synchronize(self.dev)
+        st = mla.read_status(self.dec.workspace)
+        if st != 0:
+            raise RuntimeError(f"{self.c.name}: device status after warm-up: {mla.status_string(st)}")
+        self.step = capture(self.eager_step, self.dev)
+        self.step_mode = "graph" if self.step is not None else "eager"
+        self.step = self.step or self.eager_step
+        self.attend = capture(self.eager_attend, self.dev) or self.eager_attend
+        if mla.read_status(self.dec.workspace) != 0:
+            raise RuntimeError(f"{self.c.name}: device status after the captured calls")
+
+    def release(self):
+        for k in ("dec", "d", "inp", "step", "attend", "eager_step", "eager_attend"):
+            if hasattr(self, k):
+                delattr(self, k)
+        torch.cuda.empty_cache()
+
+
+def config_line(run, steps, stream, dev, flush, pk):
+    """Step time, attention time (each from its graph), roofline and rates of one
+    secondary workload; short, for the default run's `configs` key."""
+    w = run.w
+    fl = flush if w["cache_bytes"] < 2 * L2_BYTES else None
+    step_ms = statistics.median(_timed_steps(run.step, steps, fl, stream, dev))
+    attn_ms = statistics.median(_timed_steps(run.attend, steps, fl, stream, dev))
+    roof = roofline_of(w, attn_ms, pk)
+    return {"workload": workload_name(run.c), "steps": steps, "ms_per_step": step_ms, "kernel_us": attn_ms * 1e3,
+            "num_splits": run.splits,
+            "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "roofline_time_us")},
+            "tflops_step": w["step_flops"] / (step_ms * 1e-3) / 1e12,
+            "attn_tflops": w["attn_flops"] / (attn_ms * 1e-3) / 1e12,
+            "attn_tbps": w["attn_bytes"] / (attn_ms * 1e-3) / 1e12,
+            "attended_tokens_per_s": w["pairs"] / (step_ms * 1e-3),
+            "decode_tokens_per_s": w["tokens"] / (step_ms * 1e-3),
+            "l2": "inputs larger than L2" if fl is None else "L2 flushed between steps (256 MB write)",
+            "launch": f"median of {steps} graph replays each of the step and of the attention alone"}
+
+
+def naive_line(run, absorbed_ms, dev, stream, reps=3):
+    """The decompress-then-attend path on the same inputs (mla_naive_decode), timed
+    beside the absorbed step: wall-time ratio next to the algorithmic FLOP ratio."""
+    from mla_decode_attention_absorbed_gb300 import mla
+    from oracle import counts
+    c, d = run.c, run.d
+    lens = run.inp["seq_lens"].tolist()
+    cache = mla.make_cache(run.prob, d["kv"], d["seq_lens"], d["block_table"], c.page_size, max(lens))
+    out, lse, ws = mla.naive_decode(run.prob, d["q_nope"], d["q_rope"], cache, d["w_uk"], d["w_uv"])
+    torch.cuda.synchronize(dev)
+    if mla.read_status(ws) != 0:
+        raise RuntimeError("naive path: device status")
+    call = lambda: mla.naive_decode(run.prob, d["q_nope"], d["q_rope"], cache, d["w_uk"], d["w_uv"],  # noqa: E731
+                                    out=out, lse=lse, workspace=ws)
+    ms = statistics.median(_timed_steps(call, reps, None, stream, dev))
+    nf = counts.naive_flops(c.H, c.d_c, c.d_rope, c.d_nope, c.d_v, lens, c.s_q)
+    af = run.w["step_flops"]
+    res = {"workload": workload_name(c), "ms": ms, "absorbed_ms": absorbed_ms, "ratio_wall": ms / absorbed_ms,
+           "flops": nf, "absorbed_flops": af, "ratio_flops": nf / af, "tflops": nf / (ms * 1e-3) / 1e12,
+           "workspace_gb": ws.numel() / 1e9, "reps": reps,
+           "path": "tcgen05 expansion GEMM (K_h, V_h of every cached token and head) + per-head attention"}
+    del out, lse, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def naive_oracle_line(budget_s=12.0):
+    """The naive form of the fp64 oracle on the host cores: the whole tiny workload,
+    and a seeded subset of the long workload's query rows (each row re-expands its
+    head's K and V over the whole history); rates of the sample, no extrapolation."""
+    import numpy as np
+
+    import oracle
+    from oracle import counts
+    res = {"cores": oracle.threads(), "kind": "oracle"}
+    tiny = CONFIGS["tiny"]
+    inp = make_inputs(tiny)
+    t = time.perf_counter()
+    oracle.naive(tiny, inp["q_nope"], inp["q_rope"], inp["kv"], inp["seq_lens"], inp["w_uk"], inp["w_uv"])
+    t = time.perf_counter() - t
+    f = counts.naive_flops(tiny.H, tiny.d_c, tiny.d_rope, tiny.d_nope, tiny.d_v, inp["seq_lens"].tolist(), tiny.s_q)
+    res["tiny"] = {"seconds": t, "tflops": f / t / 1e12, "sample": "the whole workload"}
+    long = CONFIGS["long"].with_(B=1)
+    inp = make_inputs(long)
+    rows_total = long.s_q * long.H
+    n = max(1, min(rows_total, oracle.threads()))
+    rows = sorted(np.random.default_rng(3).choice(rows_total, size=n, replace=False).tolist())
+    t = time.perf_counter()
+    oracle.naive(long, inp["q_nope"], inp["q_rope"], inp["kv"], inp["seq_lens"], inp["w_uk"], inp["w_uv"], rows=rows)
+    t = time.perf_counter() - t
+    L = int(inp["seq_lens"][0])
+    per_row = counts.naive_flops(1, long.d_c, long.d_rope, long.d_nope, long.d_v, [L], long.s_q)
+    res["long"] = {"seconds": t, "tflops": per_row * n / t / 1e12,
+                   "sample": f"{n} seeded query rows of the first sequence (L={L}), each re-expanding its head"}
+    return res
+
+
 def run_ours(cfg, args, rank, world, local, active):
     from mla_decode_attention_absorbed_gb300 import mla
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     mla.load()
-    c = cfg.with_(seed=replica_seed(cfg.seed, rank))
-    inp = make_inputs(c)
-    kv_scale = None
-    if args.kv == "fp8":
-        inp["kv"] = to_fp8_cache(inp["kv"])
-        kv_scale = inp["kv_scale"] = KV_FP8_SCALE
-    w = work(c, inp["seq_lens"].tolist(), 1 if args.kv == "fp8" else 2)
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    prob = mla.Problem.of(c)
-    dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], c.page_size,
-                      max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=kv_scale)
-    splits = mla.decode_num_splits(prob, dec.cache) if args.splits == 0 else args.splits
-    q_nope, q_rope = d["q_nope"], d["q_rope"]
     stream = torch.cuda.current_stream(dev)
-
-    flush = None
-    if w["cache_bytes"] < 2 * L2_BYTES:
-        flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
-
-    def eager_step():
-        dec.step(q_nope, q_rope)  # mla_decode_step: absorb -> attention -> out_proj, launches overlapping
-
-    for _ in range(args.warmup):
-        if flush is not None:
-            flush.zero_()
-        eager_step()
-    torch.cuda.synchronize(dev)
-    st = mla.read_status(dec.workspace)
-    if st != 0:
-        raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
-    # The timed steps replay the step captured as a CUDA graph (the same three
-    # launches, with their programmatic overlap), so that the host's launch work
-    # does not open gaps between them; where capture is refused they run eagerly.
-    step_graph = torch.cuda.CUDAGraph()
-    step_mode = "graph"
-    try:
-        with torch.cuda.graph(step_graph, capture_error_mode="relaxed"):
-            eager_step()
-        step_graph.replay()
-        torch.cuda.synchronize(dev)
-        if mla.read_status(dec.workspace) != 0:
-            raise RuntimeError("device status after the captured step")
-    except RuntimeError:
-        torch.cuda.synchronize(dev)
-        step_mode = "eager"
-
-    def step():
-        if step_mode == "graph":
-            step_graph.replay()
-        else:
-            eager_step()
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    run = DecodeRun(cfg, args, rank, dev, args.kv)
+    w = run.w
+    fl = flush if w["cache_bytes"] < 2 * L2_BYTES else None
+    run.warm(args.warmup, fl)
+    step = run.step
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(local).start()
-    soak(step, dev, 1.0, flush)
+    clocks = ClockSampler(nvsmi_gpu_id(local)).start()
+    soak(step, dev, 1.0, fl)
     barrier(active)
     torch.cuda.synchronize(dev)
     t_wall = time.perf_counter()
     for k in range(K):
-        if flush is not None:
-            flush.zero_()
+        if fl is not None:
+            fl.zero_()
         ev[k][0].record(stream)
         step()
         ev[k][1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(active)
     t_wall = time.perf_counter() - t_wall
-    # the attention kernel alone (its own launch, same inputs), for its roofline
-    for k in range(K):
-        if flush is not None:
-            flush.zero_()
-        ev_attn[k][0].record(stream)
-        dec.attend()
-        ev_attn[k][1].record(stream)
-    torch.cuda.synchronize(dev)
+    # the attention kernel alone (its own launch from a graph, same inputs), for its roofline
+    attn_ms_list = _timed_steps(run.attend, K, fl, stream, dev)
     clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    attn_ms = [a.elapsed_time(b) for a, b in ev_attn]
     ms_local = sum(step_ms) / K
     ms = reduce_max(ms_local, active, "cuda" if active and args.backend == "nccl" else "cpu")
-    attn_avg = sum(attn_ms) / K
+    attn_avg = sum(attn_ms_list) / K
 
     # end to end through the public API: every step copies its inputs from pinned host
     # memory (queries, lengths, block table) and reads its result back
+    c, d, inp, prob = run.c, run.d, run.inp, run.prob
+    q_nope, q_rope = d["q_nope"], d["q_rope"]
     h_qn = inp["q_nope"].pin_memory()
     h_qr = inp["q_rope"].pin_memory()
     h_lens = inp["seq_lens"].pin_memory()
@@ -313,7 +447,7 @@ def run_ours(cfg, args, rank, world, local, active):
         lens_j = d["seq_lens"].clone()
         bt_j = d["block_table"].clone() if d["block_table"] is not None else None
         dec_j = mla.Decoder(prob, d["kv"], lens_j, d["w_uk"], d["w_uv"], bt_j, c.page_size,
-                            max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=kv_scale)
+                            max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=run.kv_scale)
         qn_j, qr_j = torch.empty_like(q_nope), torch.empty_like(q_rope)
         sets.append(dict(dec=dec_j, ins=[qn_j, qr_j, lens_j] + ([bt_j] if bt_j is not None else []),
                          out=dec_j.out, h_out=torch.empty(dec_j.out.shape, dtype=dec_j.out.dtype).pin_memory(),
@@ -327,14 +461,27 @@ def run_ours(cfg, args, rank, world, local, active):
     e2e_ms = reduce_max(e2e_local, active, "cuda" if active and args.backend == "nccl" else "cpu")
     if any(mla.read_status(sj["dec"].workspace) != 0 for sj in sets):
         raise RuntimeError("device status after the end-to-end loop")
-
-    # parity spot check of the timed configuration (a few rows against the oracle)
-    return dict(w=w, ms=ms, attn_ms=attn_avg, e2e_ms=e2e_ms, e2e_mode=e2e_mode + " (%d steps)" % e2e_steps,
-                step_mode=step_mode,
-                h2d=h2d, d2h=d2h, splits=splits, clocks=clocks,
-                step_ms=step_ms, wall_s=t_wall, inp=inp, c=c, launches_per_step=3 + (1 if splits > 1 else 0))
-
-
+    del sets
+    res = dict(w=w, ms=ms, attn_ms=attn_avg, e2e_ms=e2e_ms, e2e_mode=e2e_mode + " (%d steps)" % e2e_steps,
+               step_mode=run.step_mode, h2d=h2d, d2h=d2h, splits=run.splits, clocks=clocks,
+               step_ms=step_ms, attn_ms_list=attn_ms_list, wall_s=t_wall, inp=inp, c=c,
+               launches_per_step=3 + (1 if run.splits > 1 else 0))
+    run.release()
+    # the other workloads of the method, each on its own (this rank's replica)
+    configs, naive = {}, None
+    if not args.headline_only and args.kv == "bf16" and cfg.name == DEFAULT_CONFIG:
+        pk = peaks()
+        steps = max(3, min(K, 20))
+        for name in SECONDARY:
+            r2 = DecodeRun(CONFIGS[name], args, rank, dev, "bf16")
+            fl2 = flush if r2.w["cache_bytes"] < 2 * L2_BYTES else None
+            r2.warm(3, fl2)
+            configs[name] = config_line(r2, steps, stream, dev, flush, pk)
+            if name == "long" and not args.no_naive:
+                naive = naive_line(r2, configs[name]["ms_per_step"], dev, stream)
+            r2.release()
+    res["configs"], res["naive"] = configs, naive
+    return res
 def cpu_baseline(cfg, inp, budget_s: float = 12.0):
     """The oracle as it stands, absorbed form, on whole sequences of the same
     workload until about ``budget_s`` of host time is spent."""
@@ -367,11 +514,16 @@ def cpu_baseline(cfg, inp, budget_s: float = 12.0):
                       f"{t_used:.1f} s"}
 
 
-def workload_name(cfg):
+def workload_name(cfg, kv: str = "bf16"):
     lens = f"T={cfg.T}" if not cfg.len_lo else f"L~U[{cfg.len_lo},{cfg.len_hi}]"
     lay = f"paged{cfg.page_size}" if cfg.paged else "contiguous"
+    cache = "bf16 cache" if kv == "bf16" else "FP8 E4M3 cache (scale 1/16)"
     return (f"{cfg.name}: B={cfg.B} H={cfg.H} d_c={cfg.d_c} d_rope={cfg.d_rope} d_nope={cfg.d_nope} "
-            f"d_v={cfg.d_v} {lens} s_q={cfg.s_q} {lay} bf16")
+            f"d_v={cfg.d_v} {lens} s_q={cfg.s_q} {lay} {cache}")
+
+
+# the other workloads of the method, each measured in the default run beside the headline
+SECONDARY = ("tiny", "long", "spec", "ragged_paged")
 
 
 def main_ours(args):
@@ -385,25 +537,18 @@ def main_ours(args):
     pk = peaks()
     total_flops = w["step_flops"] * world
     value = total_flops / (ms * 1e-3) / 1e12
-    tensor_bound = w["attn_flops"] / (pk["bf16_tflops"] * 1e12) > w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)
-    attn_s = r["attn_ms"] * 1e-3
-    if tensor_bound:
-        achieved = w["attn_flops"] / attn_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_tflops"]}
-    else:
-        achieved = w["attn_bytes"] / attn_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"]}
+    roof = roofline_of(w, r["attn_ms"], pk)
     roof["traffic"] = traffic_for(f"attn{'_fp8' if args.kv == 'fp8' else ''}:{cfg.name}")
     roof["kernel"] = "mla_decode_attn (split-T attention + LSE combine)" + (
         ", FP8 E4M3 cache dequantised on chip, fp16 MMAs" if args.kv == "fp8" else "")
-    roof["peak_source"] = pk["source"] + (" burst bf16" if tensor_bound else " HBM copy")
-    roof["roofline_time_us"] = max(w["attn_flops"] / (pk["bf16_tflops"] * 1e12),
-                                   w["attn_bytes"] / (pk["hbm_gbs"] * 1e9)) * 1e6
-    roof["kernel_us"] = r["attn_ms"] * 1e3
+    roof["kernel_timing"] = (f"CUDA events around each of {args.steps} replays of the attention call captured "
+                             "as a CUDA graph (no host launch work inside)")
     cpu = cpu_baseline(r["c"], r["inp"], args.cpu_budget) if not args.no_cpu_baseline else None
+    naive = r["naive"]
+    if naive is not None and not args.no_cpu_baseline:
+        naive["oracle"] = naive_oracle_line()
     clk = r["clocks"].summary()
+    attn_s = r["attn_ms"] * 1e-3
     line = {
         "metric": METRIC,
         "value": value,
@@ -417,7 +562,7 @@ def main_ours(args):
         "vs_baseline": None,
         "dtype": "bf16" if args.kv == "bf16" else "e4m3 cache, f16 MMAs, bf16 projections",
         "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights)",
-        "config": {"workload": workload_name(cfg) + (", FP8 E4M3 cache (scale 1/16)" if args.kv == "fp8" else ""),
+        "config": {"workload": workload_name(cfg, args.kv),
                    "num_splits": r["splits"],
                    "l2": ("inputs larger than L2: the cache alone is "
                           f"{w['cache_bytes'] / 1e6:.0f} MB per replica") if w["cache_bytes"] >= 2 * L2_BYTES
@@ -443,6 +588,8 @@ def main_ours(args):
         "clocks": clk,
         "step_ms_min": min(r["step_ms"]),
         "step_ms_median": statistics.median(r["step_ms"]),
+        "configs": r["configs"],
+        "naive": naive,
     }
     print(json.dumps(line))
 
@@ -653,8 +800,7 @@ def main_op(args):
         "vs_baseline": None,
         "dtype": "bf16" if args.kv == "bf16" else "bf16 GEMM, e4m3 cache rows",
         "data": "synthetic (seeded N(0,1) hidden states, N(0,1/d_model) W_DKV)",
-        "config": {"workload": f"append to {workload_name(c)}, d_model={D_MODEL}"
-                               + (", FP8 E4M3 cache (scale 1/16)" if args.kv == "fp8" else ""),
+        "config": {"workload": f"append to {workload_name(c, args.kv)}, d_model={D_MODEL}",
                    "l2": "L2 flushed between steps (256 MB write)",
                    "launch": "the step's kernels replayed as a CUDA graph",
                    "parallelism": f"{world} independent replica(s)"},
@@ -973,8 +1119,7 @@ def main_sparse(args, cfg, rank, world, local, active):
         "vs_baseline": None,
         "dtype": "bf16" if args.kv == "bf16" else "e4m3 cache, f16 MMAs, bf16 projections",
         "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights, uniform random top-k lists)",
-        "config": {"workload": f"{workload_name(c)}, top-{TOPK} lists"
-                               + (", FP8 E4M3 cache (scale 1/16)" if args.kv == "fp8" else ""),
+        "config": {"workload": f"{workload_name(c, args.kv)}, top-{TOPK} lists",
                    "num_splits": args.splits,
                    "l2": "L2 flushed between steps (256 MB write)",
                    "parallelism": f"{world} independent replica(s), sequences sharded by rank"},
@@ -1064,6 +1209,9 @@ def parse(argv=None):
     ap.add_argument("--backend", default="nccl", choices=["nccl", "gloo"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="decode: time the headline workload only (no `configs`, no naive leg)")
+    ap.add_argument("--no-naive", action="store_true", help="decode: skip the naive comparison leg")
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
                     help="latent cache format of the decode and sparse ops (fp8: E4M3 codes, scale 1/16)")
     ap.add_argument("--op", default="decode", choices=["decode", "append", "sparse", "prefill"],
