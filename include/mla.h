@@ -289,6 +289,16 @@ MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, con
                                     void *o_lat, float *lse, int num_splits, int *device_status,
                                     void *stream);
 
+/* Diagnostics (the pages have no counterpart): the bound, in nanoseconds, of
+ * every wait for work inside the attention kernels launched from now on by this
+ * process (mla_decode_attn, mla_decode_step, the sparse, prefill and no-alloc
+ * entry points).  A wait that runs out records MLA_ERR_TIMEOUT in the status
+ * word; the kernel then drains the copies and MMAs it has in flight (those waits
+ * keep the default bound) and returns, outputs undefined.  0 restores the
+ * default, 2 s.  For tests of the timeout path and for diagnosing a stalled GPU;
+ * not for production use.  Always returns MLA_OK. */
+MLA_API int mla_set_wait_limit_ns(unsigned long long ns);
+
 /* One whole absorbed decode step: mla_absorb_q -> mla_decode_attn ->
  * mla_out_proj with one call, the same arguments and results (q_cat and o_lat
  * are the caller's intermediate buffers, the workspace is sized by

@@ -4,6 +4,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -11,6 +13,10 @@ namespace {
 
 constexpr int kAbiVersion = 2;
 constexpr int kMaxSplits = 64;
+// Bound of the attention kernels' waits for work, set by mla_set_wait_limit_ns
+// (0: the kernels' default).
+std::atomic<unsigned long long> g_wait_ns{0};
+
 // SMs of the current device (split planning only), looked up once per device
 int num_sms() {
     static int cached[64] = {0};
@@ -257,6 +263,7 @@ mla::AttnParams make_params(const mla_dims *d, const mla_cache *c) {
     p.block_table = c->block_table;
     p.max_pages = c->max_pages; p.page_size = c->page_size; p.num_pages = c->num_pages;
     p.seq_lens = c->seq_lens;
+    p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     return p;
 }
 
@@ -323,6 +330,11 @@ MLA_API const char *mla_status_string(int status) {
 }
 
 MLA_API int mla_abi_version(void) { return kAbiVersion; }
+
+MLA_API int mla_set_wait_limit_ns(unsigned long long ns) {
+    g_wait_ns.store(ns, std::memory_order_relaxed);
+    return MLA_OK;
+}
 
 MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q_rope, const void *w_uk,
                          void *q_cat, void *stream) {

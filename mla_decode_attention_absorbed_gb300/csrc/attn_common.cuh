@@ -21,17 +21,23 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Bounded wait that also gives up once the CTA is aborting (S: the kernel's
-// shared-memory block, with an `abort` flag).
+// shared-memory block, with an `abort` flag and the launch's wait bound
+// `wait_ns`; the cycle bound is twice it, about the SM clock in GHz, so the
+// bound holds even if one of the two clocks does not advance).
 template <bool kCluster = false, class S>
 __device__ __forceinline__ bool wait_bar(S &sm, uint64_t *bar, uint32_t parity) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     const long long c0 = clock64();
+    const uint64_t lim_ns = sm.wait_ns;
+    const long long lim_cyc = (long long)(lim_ns > (1ull << 61) ? (1ull << 62) : 2 * lim_ns);
     for (uint32_t it = 1;; ++it) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
+        // the clocks are read after the first retry (a try_wait suspends in hardware,
+        // so a short bound is seen at once) and then every 64
+        if (it == 1 || (it & 63u) == 0) {
             if (*(volatile int *)&sm.abort) return false;
-            if (wait_expired(t0, c0)) return false;
+            if (globaltimer_ns() - t0 > lim_ns || clock64() - c0 > lim_cyc) return false;
         }
     }
 }

@@ -153,6 +153,7 @@ struct Smem {
     uint64_t staged, tx_free, rx_full[2];
     uint32_t tmem_base;
     int abort;    // set by this CTA or, remotely, by the peer
+    uint64_t wait_ns;  // bound of the waits for work (the launch's, else the default)
     int lpt_b, lpt_L;  // longest-first order: the sequence of this CTA's work item, its length
     int armed;    // last tile whose receive the exchange warp armed
     int received; // last tile the softmax warps received
@@ -333,6 +334,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         mbar_init(&sm.rx_full[1], 1);
         for (int q = 0; q < 4; ++q) sm.pair_stop[q][0] = sm.pair_stop[q][1] = 0;
         sm.abort = 0;
+        sm.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
         sm.armed = sm.received = -1;
         fence_mbar_init();
         tma_prefetch_desc(&tm0);

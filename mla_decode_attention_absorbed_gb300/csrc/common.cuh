@@ -51,6 +51,10 @@ struct AttnParams {
     // decode step): q_cat is read only once that grid has completed, and the next
     // grid (out_proj) may start its CTAs at once
     int pdl;
+    // bound of the kernel's waits for work (0: the default, 2 s); a wait that runs
+    // out records MLA_ERR_TIMEOUT and the CTA unwinds (the waits that drain copies
+    // and MMAs still in flight keep the default)
+    unsigned long long wait_ns;
 };
 
 // Record the first device-side error; later ones keep the first.

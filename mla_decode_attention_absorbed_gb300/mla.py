@@ -45,7 +45,7 @@ EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_w
            "mla_naive_decode", "mla_read_status", "mla_decode_attn_noalloc", "mla_cache_append_workspace_size",
            "mla_cache_append", "mla_decode_sparse_workspace_size", "mla_decode_attn_sparse", "mla_prefill_crossover",
            "mla_prefill_expand_workspace_size", "mla_prefill_expand", "mla_prefill_workspace_size", "mla_prefill",
-           "mla_decode_step")
+           "mla_decode_step", "mla_set_wait_limit_ns")
 PATH_ABSORB, PATH_EXPAND = 0, 1
 
 
@@ -105,6 +105,8 @@ def load(path: str | None = None):
     lib.mla_prefill.restype = I
     lib.mla_decode_attn_noalloc.argtypes = [pd, P, pc, P, P, I, P, P]
     lib.mla_decode_attn_noalloc.restype = I
+    lib.mla_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.mla_set_wait_limit_ns.restype = I
     if path is None:
         _lib = lib
     return lib
@@ -361,6 +363,12 @@ def decode_attn_noalloc(prob: Problem, q_cat, cache: Cache, o_lat, lse, num_spli
                                           _ptr(lse), int(num_splits), _ptr(device_status), _stream(stream)),
            "mla_decode_attn_noalloc")
     return o_lat, lse
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """mla_set_wait_limit_ns: the bound of the attention kernels' waits for work
+    (0: the default 2 s).  For tests of the timeout path."""
+    _check(load().mla_set_wait_limit_ns(int(ns)), "mla_set_wait_limit_ns")
 
 
 def read_status(workspace, stream=None) -> int:

@@ -95,3 +95,27 @@ def test_host_errors_raise():
     with pytest.raises(mla.MLAError) as e:
         mla.absorb_q(prob, d["q_nope"], d["q_rope"], d["w_uk"], q_cat=mis)
     assert e.value.code == 4
+
+
+def test_wait_timeout_reported_and_recovered():
+    """A bounded wait that runs out: with the attention kernels' wait bound set to
+    1 ns (the tiny workload, one CTA per work item), some wait for work gives up,
+    the kernel records MLA_ERR_TIMEOUT, drains its copies and MMAs in flight (those
+    waits keep the 2 s bound) and returns; the next call, with the default bound
+    restored, runs clean and matches the oracle."""
+    from mla_decode_attention_absorbed_gb300.workloads import CONFIGS
+    cfg = CONFIGS["tiny"]
+    inp = make_inputs(cfg)
+    d = to_dev(inp)
+    prob, cache = gpu_cache(cfg, d)
+    q_cat = mla.absorb_q(prob, d["q_nope"], d["q_rope"], d["w_uk"])
+    try:
+        mla.set_wait_limit_ns(1)
+        _, _, ws = mla.decode_attn(prob, q_cat, cache)
+        torch.cuda.synchronize()
+        assert mla.read_status(ws) == 8  # MLA_ERR_TIMEOUT
+    finally:
+        mla.set_wait_limit_ns(0)
+    g = run_gpu(cfg, inp)
+    assert g["status"] == 0
+    check_against_oracle(cfg, inp, g)
