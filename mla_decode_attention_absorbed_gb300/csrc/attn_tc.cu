@@ -16,14 +16,18 @@
 // key.  Each CTA loads only its own channel slice of every tile and computes
 // the partial score over that slice; the pair swaps partial scores (sent as
 // fp16) with one bulk shared-memory copy per tile and direction, and each CTA
-// adds the peer's to its own fp32 partial.  The swap of tile n+1 is in flight
-// while tile n's softmax runs.  Each CTA then runs the softmax of all rows and
-// accumulates its half of O; its running (m, l) describe that half (the two
-// CTAs' scores differ only by the fp16 rounding of the other CTA's partial,
-// so split partials carry one (m, l) per CTA).  A CTA ships tile n+1 only after it has received
-// and consumed the peer's tile n, so with two receive buffers (by tile parity)
-// a buffer is never refilled before it has been read, and no "buffer free"
-// signal has to cross the cluster.
+// adds the peer's to its own fp32 partial.  Each CTA then runs the softmax of
+// all rows and accumulates its half of O; its running (m, l) describe that half
+// (the two CTAs' scores differ only by the fp16 rounding of the other CTA's
+// partial, so split partials carry one (m, l) per CTA).  The swap of tile n+1
+// is in flight while tile n's softmax runs.  Send and receive buffers are
+// double (by tile parity).  A copy into the peer completes only on the peer's
+// barrier, so the peer's softmax warps tell the sender when they have consumed
+// tile n (an arrive on the sender's barrier, across the cluster): that frees
+// the peer's receive buffer for tile n+2 and the sender's staging buffer of
+// tile n.  (Staging tile n+1 before waiting for the peer's tile n, which takes
+// the swap's round trip off the loop, measured slower: the softmax of tile n,
+// on which the operand ring waits, then starts later.)
 //
 // Three ways of feeding the tensor cores.
 //  - Dense bf16 cache: the producer's TMA tile loads write the 128-byte-swizzled
@@ -137,9 +141,9 @@ struct Geo {
 struct Smem {
     uint8_t kv[kRing][kStageBytes];  // swizzled operand tiles (FP8: raw codes first land at the top)
     // split mode: this CTA's scaled partial scores (fp16) staged for the bulk copy
-    // to the peer, and the peer's received by tile parity.  Row r is 128 B (64
-    // fp16); its 16-byte chunk c sits at chunk c ^ (r % 8).
-    alignas(128) __half tx[kRows * kTile];
+    // to the peer, and the peer's received, both by tile parity.  Row r is 128 B
+    // (64 fp16); its 16-byte chunk c sits at chunk c ^ (r % 8).
+    alignas(128) __half tx[2][kRows * kTile];
     __half rx[2][kRows * kTile];
     // per half-row values the two warps of a quadrant exchange, by tile parity:
     // tile maxima in the loop, softmax sums in the epilogue
@@ -150,7 +154,10 @@ struct Smem {
     uint64_t full[kRing], empty[kRing];
     uint64_t landed[kRing], read[kRing];  // FP8: raw codes landed; every converter holds its codes
     uint64_t q_ready, s_full, s_free, p_ready, o_done, drain;
-    uint64_t staged, tx_free, rx_full[2];
+    // staged[i]: the softmax warps staged the tile of parity i; rx_full[i]: the
+    // peer's tile of parity i landed; peer_free[i]: the peer's softmax warps
+    // consumed this CTA's tile of parity i (arrived on from the peer)
+    uint64_t staged[2], rx_full[2], peer_free[2];
     uint32_t tmem_base;
     int abort;    // set by this CTA or, remotely, by the peer
     uint64_t wait_ns;  // bound of the waits for work (the launch's, else the default)
@@ -158,6 +165,9 @@ struct Smem {
     int armed;    // last tile whose receive the exchange warp armed
     int received; // last tile the softmax warps received
 };
+
+// the whole block, with no realignment slack, within the 227 KB a CTA may use
+static_assert(sizeof(Smem) <= 232448, "shared memory block over the per-CTA limit");
 
 // This thread's 32 scores of the tile in S (tensor memory).
 __device__ __forceinline__ void load_scores(uint32_t taddr, float (&s)[kHalf]) {
@@ -273,8 +283,16 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     constexpr int kExch = kExchangeWarp;
     constexpr int kNConv = kStaged ? kFp8ConvWarps : kConvWarps;
     constexpr bool kRegSplit = threads_of(kSparse, kFp8) == 512;
-    extern __shared__ uint8_t smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // the launch reserves no slack for realignment (the block is within a few
+    // hundred bytes of the limit): a window that does not start on a 1 KB
+    // boundary (the swizzled operand tiles need one) is reported, not used;
+    // both CTAs of a pair see the same offset, so both leave here
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) set_status(p.status, MLA_ERR_UNSUPPORTED);
+        return;
+    }
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (p.pdl) pdl_launch_dependents();
@@ -328,10 +346,11 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         mbar_init(&sm.p_ready, kSoftmaxThreads);
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.drain, 2);  // one commit from each MMA issuer
-        mbar_init(&sm.staged, kSoftmaxThreads);
-        mbar_init(&sm.tx_free, 1);
-        mbar_init(&sm.rx_full[0], 1);
-        mbar_init(&sm.rx_full[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.staged[i], kSoftmaxThreads);
+            mbar_init(&sm.rx_full[i], 1);
+            mbar_init(&sm.peer_free[i], kSoftmaxWarps);  // one arrive per softmax warp of the peer
+        }
         for (int q = 0; q < 4; ++q) sm.pair_stop[q][0] = sm.pair_stop[q][1] = 0;
         sm.abort = 0;
         sm.wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
@@ -351,7 +370,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         // (length descending, index ascending), so that over several waves the long
         // sequences start first and the short ones fill in behind them; every CTA
         // ranks the lengths itself (B is small: the host enables this up to 1024)
-        int *lens = reinterpret_cast<int *>(sm.tx);
+        int *lens = reinterpret_cast<int *>(sm.tx[0]);
 #pragma unroll
         for (int k = 0; k < kLensPerThread; ++k) {
             const int c = threadIdx.x + k * blockDim.x;
@@ -624,22 +643,26 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         } else if (warp == kExch) {
             // ------------------------------------------------------------ score exchange (split mode)
             // Ships each staged tile of partial scores to the peer with one bulk copy
-            // that completes on the peer's receive barrier, then frees the staging buffer.
+            // that completes on the peer's receive barrier of the tile's parity, once
+            // the peer has consumed the tile two before (its buffer is then free).
+            // This CTA's own receive of tile u is armed first: the receive of tile
+            // u - 2 has completed by then (the softmax warps consume it before they
+            // stage tile u), and bytes of tile u that land before the arm only take
+            // the barrier's transaction count below zero for a while.
             if (kSplit && lane == 0) {
                 const uint32_t rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
                 const uint32_t rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
                 for (int u = 0; u < ntiles; ++u) {
-                    if (!wait_bar(sm, &sm.staged, u & 1)) {
+                    const int pb = u & 1;
+                    if (!wait_bar(sm, &sm.staged[pb], (u >> 1) & 1) ||
+                        (u >= 2 && !wait_bar<true>(sm, &sm.peer_free[pb], ((u >> 1) - 1) & 1))) {
                         raise_abort<kSplit>(sm, p, peer);
                         break;
                     }
-                    mbar_arrive_expect_tx(&sm.rx_full[u & 1], kXBytes);  // arm this CTA's receive of tile u
+                    mbar_arrive_expect_tx(&sm.rx_full[pb], kXBytes);
                     *(volatile int *)&sm.armed = u;
-                    bulk_copy_to_peer(rx_peer0 + (u & 1) * (uint32_t)sizeof(sm.rx[0]), sm.tx, kXBytes,
-                                      rxfull_peer0 + (u & 1) * (uint32_t)sizeof(uint64_t));
-                    bulk_commit();
-                    bulk_wait_read_all();
-                    mbar_arrive(&sm.tx_free);
+                    bulk_copy_to_peer(rx_peer0 + pb * (uint32_t)sizeof(sm.rx[0]), sm.tx[pb], kXBytes,
+                                      rxfull_peer0 + pb * (uint32_t)sizeof(uint64_t));
                 }
             }
         } else if (warp >= kConvWarp0 && kLoaders) {
@@ -812,7 +835,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         qv[i][k] = *reinterpret_cast<const uint4 *>(src[k] + g.qk0 + c);
                 }
             }
-            uint8_t *slot = reinterpret_cast<uint8_t *>(sm.tx) + warp * 2048;
+            uint8_t *slot = reinterpret_cast<uint8_t *>(sm.tx[0]) + warp * 2048;
 #pragma unroll
             for (int i = 0; i < kMaxBoxes; ++i) {
                 const int c0 = 32 * hf + 64 * i;
@@ -847,20 +870,21 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         const int sw = r & 7;  // chunk swizzle of this row in tx / rx
         const uint32_t s_addr = tmem + lane_base + kColS + kHalf * hf;
 
-        // Split mode: round this thread's partial scores to fp16 (kept in `own`, so
-        // both CTAs later add the same two numbers), stage them for the exchange
-        // warp and move on.
+        // Split mode: round this thread's partial scores to fp16, stage them for the
+        // exchange warp (the staging buffer of tile u is free once the peer has
+        // consumed tile u - 2, whose copy read it) and move on.
+        const uint32_t peer_free_remote0 = kSplit ? map_to_rank(smem_u32(&sm.peer_free[0]), peer) : 0u;
         auto stage = [&](int u, const float (&sp)[kHalf]) {
-            if (u >= 1 && !warp_wait(sm, &sm.tx_free, (u - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
+            if (u >= 2 && !warp_wait<true>(sm, &sm.peer_free[u & 1], ((u >> 1) - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
             uint32_t h16[kHalf / 2];
 #pragma unroll
             for (int j = 0; j < kHalf / 2; ++j) h16[j] = pack_f16x2(sp[2 * j], sp[2 * j + 1]);
-            uint4 *txrow = reinterpret_cast<uint4 *>(sm.tx + r * kTile);
+            uint4 *txrow = reinterpret_cast<uint4 *>(sm.tx[u & 1] + r * kTile);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 txrow[(4 * hf + c) ^ sw] = make_uint4(h16[4 * c], h16[4 * c + 1], h16[4 * c + 2], h16[4 * c + 3]);
             fence_proxy_async_smem();
-            mbar_arrive(&sm.staged);
+            mbar_arrive(&sm.staged[u & 1]);
         };
 
         float m2 = -INFINITY;  // running (possibly stale) row maximum, log2 units (same in both halves)
@@ -892,8 +916,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             }
             float x[kHalf];  // scaled scores of tile n
             if (kSplit) {
-                // the peer's partial of tile n; it is consumed before tile n+1 is staged,
-                // which is what lets two receive buffers suffice
+                // the peer's partial of tile n
                 if (warp_wait<true>(sm, &sm.rx_full[n & 1], (n >> 1) & 1)) {
                     if (threadIdx.x == 0) *(volatile int *)&sm.received = n;
                 } else {
@@ -911,6 +934,10 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         add_f16x2_to(w4[e], x[8 * c + 2 * e], x[8 * c + 2 * e + 1]);
                     }
                 }
+                // every lane of the warp has read its rows of the buffer (the sums above
+                // use them): tell the peer that tile n is consumed
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote_relaxed(peer_free_remote0 + (uint32_t)(n & 1) * (uint32_t)sizeof(uint64_t));
                 if (more) stage(n + 1, sn);
             } else {
 #pragma unroll
@@ -1134,7 +1161,7 @@ template <bool kSplit, bool kPaged, bool kSparse, bool kFp8>
 cudaError_t launch_variant(const CUtensorMap &tm0, const CUtensorMap &tm1, const AttnParams &p, const Geo &g0,
                            const Geo &g1, cudaStream_t st) {
     constexpr bool kStaged = kFp8;
-    const int smem = (int)sizeof(Smem) + 1024;
+    const int smem = (int)sizeof(Smem);
     auto kern = attn_tc<kSplit, kPaged, kSparse, kFp8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
