@@ -21,13 +21,16 @@
 // (the two CTAs' scores differ only by the fp16 rounding of the other CTA's
 // partial, so split partials carry one (m, l) per CTA).  The swap of tile n+1
 // is in flight while tile n's softmax runs.  Send and receive buffers are
-// double (by tile parity).  A copy into the peer completes only on the peer's
-// barrier, so the peer's softmax warps tell the sender when they have consumed
-// tile n (an arrive on the sender's barrier, across the cluster): that frees
-// the peer's receive buffer for tile n+2 and the sender's staging buffer of
-// tile n.  (Staging tile n+1 before waiting for the peer's tile n, which takes
-// the swap's round trip off the loop, measured slower: the softmax of tile n,
-// on which the operand ring waits, then starts later.)
+// double (by tile parity), and a CTA stages tile n+1 only after it has
+// received and consumed the peer's tile n.  That order frees both buffers
+// without a signal across the cluster: the peer shipped its tile n only after
+// consuming this CTA's tile n-1, whose copy had therefore finished reading the
+// staging buffer that tile n+1 now takes (a copy into the peer completes on
+// the peer's barrier alone), and the peer ships tile n+2 into a receive buffer
+// only after receiving tile n+1, which this CTA stages after consuming tile n.
+// (Staging tile n+1 before waiting for the peer's tile n, with a "consumed"
+// signal across the cluster, measured slower: the softmax of tile n, on which
+// the operand ring waits, then starts later.)
 //
 // Three ways of feeding the tensor cores.
 //  - Dense bf16 cache: the producer's TMA tile loads write the 128-byte-swizzled
@@ -155,9 +158,8 @@ struct Smem {
     uint64_t landed[kRing], read[kRing];  // FP8: raw codes landed; every converter holds its codes
     uint64_t q_ready, s_full, s_free, p_ready, o_done, drain;
     // staged[i]: the softmax warps staged the tile of parity i; rx_full[i]: the
-    // peer's tile of parity i landed; peer_free[i]: the peer's softmax warps
-    // consumed this CTA's tile of parity i (arrived on from the peer)
-    uint64_t staged[2], rx_full[2], peer_free[2];
+    // peer's tile of parity i landed
+    uint64_t staged[2], rx_full[2];
     uint32_t tmem_base;
     int abort;    // set by this CTA or, remotely, by the peer
     uint64_t wait_ns;  // bound of the waits for work (the launch's, else the default)
@@ -349,7 +351,6 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.staged[i], kSoftmaxThreads);
             mbar_init(&sm.rx_full[i], 1);
-            mbar_init(&sm.peer_free[i], kSoftmaxWarps);  // one arrive per softmax warp of the peer
         }
         for (int q = 0; q < 4; ++q) sm.pair_stop[q][0] = sm.pair_stop[q][1] = 0;
         sm.abort = 0;
@@ -643,19 +644,17 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         } else if (warp == kExch) {
             // ------------------------------------------------------------ score exchange (split mode)
             // Ships each staged tile of partial scores to the peer with one bulk copy
-            // that completes on the peer's receive barrier of the tile's parity, once
-            // the peer has consumed the tile two before (its buffer is then free).
-            // This CTA's own receive of tile u is armed first: the receive of tile
-            // u - 2 has completed by then (the softmax warps consume it before they
-            // stage tile u), and bytes of tile u that land before the arm only take
-            // the barrier's transaction count below zero for a while.
+            // that completes on the peer's receive barrier of the tile's parity.  This
+            // CTA's own receive of tile u is armed first: the receive of tile u - 2
+            // has completed by then (the softmax warps consume it before they stage
+            // tile u), and bytes of tile u that land before the arm only take the
+            // barrier's transaction count below zero for a while.
             if (kSplit && lane == 0) {
                 const uint32_t rx_peer0 = map_to_rank(smem_u32(sm.rx[0]), peer);
                 const uint32_t rxfull_peer0 = map_to_rank(smem_u32(&sm.rx_full[0]), peer);
                 for (int u = 0; u < ntiles; ++u) {
                     const int pb = u & 1;
-                    if (!wait_bar(sm, &sm.staged[pb], (u >> 1) & 1) ||
-                        (u >= 2 && !wait_bar<true>(sm, &sm.peer_free[pb], ((u >> 1) - 1) & 1))) {
+                    if (!wait_bar(sm, &sm.staged[pb], (u >> 1) & 1)) {
                         raise_abort<kSplit>(sm, p, peer);
                         break;
                     }
@@ -871,11 +870,8 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         const uint32_t s_addr = tmem + lane_base + kColS + kHalf * hf;
 
         // Split mode: round this thread's partial scores to fp16, stage them for the
-        // exchange warp (the staging buffer of tile u is free once the peer has
-        // consumed tile u - 2, whose copy read it) and move on.
-        const uint32_t peer_free_remote0 = kSplit ? map_to_rank(smem_u32(&sm.peer_free[0]), peer) : 0u;
+        // exchange warp and move on.
         auto stage = [&](int u, const float (&sp)[kHalf]) {
-            if (u >= 2 && !warp_wait<true>(sm, &sm.peer_free[u & 1], ((u >> 1) - 1) & 1)) raise_abort<kSplit>(sm, p, peer);
             uint32_t h16[kHalf / 2];
 #pragma unroll
             for (int j = 0; j < kHalf / 2; ++j) h16[j] = pack_f16x2(sp[2 * j], sp[2 * j + 1]);
@@ -934,10 +930,6 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         add_f16x2_to(w4[e], x[8 * c + 2 * e], x[8 * c + 2 * e + 1]);
                     }
                 }
-                // every lane of the warp has read its rows of the buffer (the sums above
-                // use them): tell the peer that tile n is consumed
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote_relaxed(peer_free_remote0 + (uint32_t)(n & 1) * (uint32_t)sizeof(uint64_t));
                 if (more) stage(n + 1, sn);
             } else {
 #pragma unroll

@@ -57,15 +57,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// The same with relaxed ordering: for a signal that only says "the data you sent
-// me has been read", given after the reading thread has used every value it
-// loaded (nothing of it is left to order).  The release form waits for the
-// thread's outstanding memory operations at cluster scope, about 1.4K cycles
-// a call in the attention's tile loop.
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
