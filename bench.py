@@ -739,7 +739,7 @@ def main_op(args):
     with torch.cuda.graph(graph):
         step()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local).start()
+    clocks = ClockSampler(nvsmi_gpu_id(local)).start()
     soak(graph.replay, dev, 1.0, flush)
     barrier(active)
     step_ms = _timed_steps(graph.replay, args.steps, flush, stream, dev)
@@ -873,7 +873,7 @@ def main_prefill(args, cfg, rank, world, local, active):
     st = mla.read_status(ws)
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {mla.status_string(st)}")
-    clocks = ClockSampler(local).start()
+    clocks = ClockSampler(nvsmi_gpu_id(local)).start()
     soak(step, dev, 1.0, flush)
     barrier(active)
     step_ms = _timed_steps(step, args.steps, flush, stream, dev)
@@ -1048,7 +1048,7 @@ def main_sparse(args, cfg, rank, world, local, active):
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     ev_a = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    clocks = ClockSampler(local).start()
+    clocks = ClockSampler(nvsmi_gpu_id(local)).start()
     soak(lambda: (absorb(), attend(), project()), dev, 1.0, flush)
     barrier(active)
     torch.cuda.synchronize(dev)
