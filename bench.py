@@ -124,7 +124,7 @@ def traffic_for(kernel_key: str):
 # headers it includes, the merge, and the entry points that choose grid and plan.
 # A change elsewhere (the projections, the expansion, the naive path) leaves the
 # attention kernel, and so its captured DRAM traffic, as it was.
-ATTN_SOURCES = ("api.cu", "attn_common.cuh", "attn_tc.cu", "combine.cu", "common.cuh", "launch.h", "sm100.cuh", "tmap.h")
+ATTN_SOURCES = ("api.cu", "attn_common.cuh", "attn_tc.cu", "attn_tc.cuh", "combine.cu", "common.cuh", "launch.h", "sm100.cuh", "tmap.h")
 
 
 def source_hash() -> str:
