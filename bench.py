@@ -124,7 +124,7 @@ def traffic_for(kernel_key: str):
 # headers it includes, the merge, and the entry points that choose grid and plan.
 # A change elsewhere (the projections, the expansion, the naive path) leaves the
 # attention kernel, and so its captured DRAM traffic, as it was.
-ATTN_SOURCES = ("api.cu", "attn_common.cuh", "attn_tc.cu", "attn_tc.cuh", "combine.cu", "common.cuh", "launch.h", "sm100.cuh", "tmap.h")
+ATTN_SOURCES = ("api.cu", "attn_common.cuh", "attn_persist.cu", "attn_tc.cu", "attn_tc.cuh", "combine.cu", "common.cuh", "launch.h", "sm100.cuh", "tmap.h")
 
 
 def source_hash() -> str:
@@ -271,6 +271,21 @@ def roofline_of(w, attn_ms, pk):
 
 
 # ------------------------------------------------------------------------- our arm
+def plan_is_balanced(prob, cache, splits):
+    """Whether mla_decode_attn runs the balanced plan for this split request: asked
+    for, or the library's choice when its workspace is the balanced plan's."""
+    from mla_decode_attention_absorbed_gb300 import mla
+    if splits == mla.SPLITS_BALANCED:
+        return True
+    if splits != 0:
+        return False
+    try:
+        bal = mla.decode_workspace_size(prob, cache, mla.SPLITS_BALANCED)
+    except ValueError:  # not available for these dims
+        return False
+    return mla.decode_workspace_size(prob, cache, 0) == bal
+
+
 class DecodeRun:
     """One decode workload on this rank's GPU: inputs, a Decoder, and the decode
     step and the attention alone each captured as a CUDA graph."""
@@ -289,6 +304,9 @@ class DecodeRun:
         self.dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], c.page_size,
                                max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=self.kv_scale)
         self.splits = mla.decode_num_splits(prob, self.dec.cache) if args.splits == 0 else args.splits
+        self.balanced = plan_is_balanced(prob, self.dec.cache, args.splits)
+        self.plan = (f"balanced ({self.splits} tile ranges per 128-row block)" if self.balanced
+                     else f"split plan ({self.splits} pieces a split sequence)" if self.splits > 1 else "unsplit")
         self.dev = dev
         self.eager_step = lambda: self.dec.step(d["q_nope"], d["q_rope"])
         self.eager_attend = lambda: self.dec.attend()
@@ -327,7 +345,7 @@ def config_line(run, steps, stream, dev, flush, pk):
     attn_ms = statistics.median(_timed_steps(run.attend, steps, fl, stream, dev))
     roof = roofline_of(w, attn_ms, pk)
     return {"workload": workload_name(run.c), "steps": steps, "ms_per_step": step_ms, "kernel_us": attn_ms * 1e3,
-            "num_splits": run.splits,
+            "num_splits": run.splits, "plan": run.plan,
             "roofline": {k: roof[k] for k in ("bound", "achieved", "peak", "unit", "frac", "roofline_time_us")},
             "tflops_step": w["step_flops"] / (step_ms * 1e-3) / 1e12,
             "attn_tflops": w["attn_flops"] / (attn_ms * 1e-3) / 1e12,
@@ -465,7 +483,7 @@ def run_ours(cfg, args, rank, world, local, active):
     res = dict(w=w, ms=ms, attn_ms=attn_avg, e2e_ms=e2e_ms, e2e_mode=e2e_mode + " (%d steps)" % e2e_steps,
                step_mode=run.step_mode, h2d=h2d, d2h=d2h, splits=run.splits, clocks=clocks,
                step_ms=step_ms, attn_ms_list=attn_ms_list, wall_s=t_wall, inp=inp, c=c,
-               launches_per_step=3 + (1 if run.splits > 1 else 0))
+               plan=run.plan, launches_per_step=3 + (1 if run.splits > 1 and not run.balanced else 0))
     run.release()
     # the other workloads of the method, each on its own (this rank's replica)
     configs, naive = {}, None
@@ -563,7 +581,7 @@ def main_ours(args):
         "dtype": "bf16" if args.kv == "bf16" else "e4m3 cache, f16 MMAs, bf16 projections",
         "data": "synthetic (seeded N(0,1) queries and latent cache, N(0,1/d_c) weights)",
         "config": {"workload": workload_name(cfg, args.kv),
-                   "num_splits": r["splits"],
+                   "num_splits": r["splits"], "plan": r["plan"],
                    "l2": ("inputs larger than L2: the cache alone is "
                           f"{w['cache_bytes'] / 1e6:.0f} MB per replica") if w["cache_bytes"] >= 2 * L2_BYTES
                    else "L2 flushed between steps (256 MB write)",

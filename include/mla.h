@@ -149,15 +149,27 @@ MLA_API int mla_abi_version(void);
 MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q_rope,
                          const void *w_uk, void *q_cat, void *stream);
 
+/* num_splits value that asks mla_decode_attn (and mla_decode_step) for the
+ * balanced plan: the batch's 64-token tiles, in batch order, dealt out in equal
+ * contiguous ranges to every CTA-pair slot of the GPU, each 128-row block of the
+ * queries its share of the slots (d_c > 256, bf16 cache, at most 4095
+ * sequences, no more 128-row blocks than slots; otherwise MLA_ERR_UNSUPPORTED).
+ * A sequence held by one range is written directly; the pieces of one cut
+ * between ranges are merged in the same launch with the same log-sum-exp
+ * combine as split pieces. */
+#define MLA_SPLITS_BALANCED (-1)
+
 /* Bytes of workspace mla_decode_attn needs for this problem and split count
- * (num_splits 0 = the library's choice).  Returns 0 for invalid arguments. */
+ * (num_splits 0 = the library's choice, MLA_SPLITS_BALANCED the balanced plan).
+ * Returns 0 for invalid or unsupported arguments. */
 MLA_API size_t mla_decode_workspace_size(const mla_dims *dims, const mla_cache *cache,
                                          int num_splits);
 
 /* Split count mla_decode_attn uses for num_splits == 0 (a function of the dims,
  * B and the max_seq_len hint only): the pieces per sequence, or, when the plan
  * splits only the sequences of a last, partly filled wave (see mla_decode_attn),
- * the pieces of those.  Returns 0 for invalid arguments. */
+ * the pieces of those; when the choice is the balanced plan, the number of
+ * equal tile ranges per 128-row block.  Returns 0 for invalid arguments. */
 MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
 
 /* Latent-space attention of every head against the shared latent cache
@@ -172,8 +184,11 @@ MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
  * parallel, each keeping an online softmax; the pieces are merged with a
  * log-sum-exp combine.  q_cat [B][s_q][H][d_c+d_rope]; o_lat [B][s_q][H][d_c];
  * lse fp32 [B][s_q][H].  num_splits 0 = the library's choice, else 1..64: every
- * sequence in num_splits pieces.  The library's choice splits every sequence
- * while the pieces fit one wave of the GPU; with more 128-row work items than a
+ * sequence in num_splits pieces; MLA_SPLITS_BALANCED the balanced plan (see
+ * there).  The library's choice splits every sequence while the pieces fit one
+ * wave of the GPU, or, with CTA pairs and a bf16 cache, takes the balanced plan
+ * when, with every sequence at max_seq_len, it gives a pair at least 16 tiles
+ * fewer than the split plan; with more 128-row work items than a
  * wave holds, it leaves them whole except those of a last, partly filled wave,
  * whose sequences (the last ones of the batch) are split to fill that wave; their
  * pieces are the last work items of the same grid.  With a bf16 cache, up to

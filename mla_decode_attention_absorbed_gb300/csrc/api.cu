@@ -31,6 +31,8 @@ int num_sms() {
 constexpr size_t kStatusBytes = 256;  // status word + padding at the workspace start
 constexpr int kMaxOrdered = 1024;     // longest-first work order up to this many sequences
 constexpr int kMaxGridZ = 65535;      // largest third grid dimension of a launch
+constexpr int kMaxPersistB = 4095;    // balanced plan: the kernel keeps the batch's tile prefix in 16 KB
+constexpr long long kBalancedMinGain = 16;  // tiles a pair the library's choice wants the balanced plan to save
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -161,33 +163,71 @@ struct DecodePlan {
     int b_tail;
     int tail_splits;
     bool lpt;  // longest sequences first (several waves of whole sequences)
+    // balanced plan (attn_persist.cu): groups of CTA pairs, each an equal range of
+    // the batch's tiles; 0 for the plans above
+    int persist_groups;
 };
 
-// The library's plan (requested == 0), else `requested` pieces for every
-// sequence.  When the work items (sequence x 128-row block) fill more than one
-// wave of clusters and the last wave is only partly used, the sequences of that
-// last wave are split over the whole of it instead: the ones before run unsplit
-// and write their rows directly, and only the tail's pieces are merged.  The
-// wave arithmetic assumes sequences of about equal length (only max_seq_len is
-// known here); with ragged lengths the tail's pieces simply start as slots free.
-// Over several waves of whole sequences the work order is longest first (the
-// kernel ranks the lengths, which only the device knows; up to 1024 sequences,
-// bf16 caches), so that a long sequence does not start in the last wave; with
-// equal lengths the order is the batch order.
-DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
+// The balanced plan (attn_persist.cu, CTA pairs, bf16 cache): every pair slot gets
+// the same share of the batch's tiles whatever the lengths and the batch size.  The
+// groups launched per 128-row block are capped by the tiles the max_seq_len hint
+// allows (at least 8 a range); the device deals out the tiles it finds.
+bool balanced_supported(const mla_dims *d, const mla_cache *c) {
     const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
-    DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1, false};
+    const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
+    const long long max_tiles = (long long)d->B * ((maxL + 63) / 64);
+    return d->d_c > 256 && c->kv_dtype == MLA_KV_BF16 && d->B <= kMaxPersistB && row_blocks <= num_sms() / 2 &&
+           max_tiles < (1ll << 31);
+}
+DecodePlan balanced_plan(const mla_dims *d, const mla_cache *c) {
+    const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
+    const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
+    const long long max_tiles = (long long)d->B * ((maxL + 63) / 64);
+    return DecodePlan{1, 0, 1, false, mla::persist_groups((int)(num_sms() / 2 / row_blocks), max_tiles)};
+}
+
+// The library's plan (requested == 0), else `requested` pieces for every
+// sequence (MLA_SPLITS_BALANCED: the balanced plan, which the caller checked is
+// supported).  In one wave of work items, the history is split to fill the wave;
+// with CTA pairs and a bf16 cache the balanced plan replaces that split when, with
+// every sequence at max_seq_len, it gives a pair at least kBalancedMinGain tiles
+// fewer (the balanced kernel's own costs, a later first score and the in-launch
+// merge, come to about that many tiles; measured: 128 -> 108 tiles a pair wins,
+// 64 -> 54 loses).  When the work items fill more than one wave of clusters and
+// the last wave is only partly used, the sequences of that last wave are split
+// over the whole of it instead: the ones before run unsplit and write their rows
+// directly, and only the tail's pieces are merged.  The wave arithmetic assumes
+// sequences of about equal length (only max_seq_len is known here); with ragged
+// lengths the tail's pieces simply start as slots free.  Over several waves of
+// whole sequences the work order is longest first (the kernel ranks the lengths,
+// which only the device knows; up to 1024 sequences, bf16 caches), so that a long
+// sequence does not start in the last wave; with equal lengths the order is the
+// batch order.
+DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
+    if (requested == MLA_SPLITS_BALANCED) return balanced_plan(d, c);
+    const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
+    const long long tiles = (maxL + 63) / 64;
     const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
     const long long units = (long long)d->B * row_blocks;
     const long long slots = d->d_c > 256 ? num_sms() / 2 : num_sms();
+    DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1, false, 0};
     pl.lpt = pl.splits == 1 && units > slots && d->B <= kMaxOrdered && c->kv_dtype == MLA_KV_BF16;
-    if (requested > 0 || pl.splits > 1) return pl;
+    if (requested > 0) return pl;
+    if (units <= slots) {
+        if (units > 0 && balanced_supported(d, c)) {
+            const DecodePlan bp = balanced_plan(d, c);
+            const long long per_split = (tiles + pl.splits - 1) / pl.splits;
+            const long long per_balanced = (d->B * tiles + bp.persist_groups - 1) / bp.persist_groups;
+            if (per_split - per_balanced >= kBalancedMinGain) return bp;
+        }
+        return pl;
+    }
     const long long rem = units % slots;
-    if (units <= slots || rem == 0) return pl;
+    if (pl.splits > 1 || rem == 0) return pl;
     const long long b_tail = (rem + row_blocks - 1) / row_blocks;
     if (b_tail >= d->B) return pl;
     long long k = slots / (b_tail * row_blocks);
-    const long long cap = ((maxL + 63) / 64) / 8;  // pieces of at least 8 tiles
+    const long long cap = tiles / 8;  // pieces of at least 8 tiles
     if (k > cap) k = cap;
     if (k > kMaxSplits) k = kMaxSplits;
     if (k < 2 || d->B - b_tail + b_tail * k > kMaxGridZ) return pl;
@@ -203,7 +243,35 @@ size_t order_bytes(const mla_dims *d, const DecodePlan &pl) {
 
 // Status word, the work order, then the split pieces' partials (only the tail's,
 // if the plan has one).
+// Balanced plan's workspace after the status block: the merge counters ([B][row
+// blocks][2], zeroed with the status word), the tile prefix (B + 1 ints), the
+// (m, l) hand-over ([pair][2 CTAs][2 item parities][128 rows][3]), the pieces'
+// (m, l) ([pair][2 slots][128 rows][2 halves][2]) and rows (bf16, [pair][2
+// slots][128 rows][d_c]).
+struct PersistLayout {
+    size_t counters, prefix, ml, part_ml, part_o, total;
+};
+PersistLayout persist_layout(const mla_dims *d, const DecodePlan &pl) {
+    const size_t n_rb = ((size_t)d->s_q * d->H + 127) / 128;
+    const size_t pairs = (size_t)pl.persist_groups * n_rb;
+    PersistLayout l;
+    l.counters = kStatusBytes;
+    l.prefix = l.counters + round_up((size_t)d->B * n_rb * 2 * sizeof(int), 256);
+    l.ml = l.prefix + round_up(((size_t)d->B + 1) * sizeof(int), 256);
+    l.part_ml = l.ml + round_up(pairs * 2 * 2 * 128 * 3 * sizeof(float), 256);
+    l.part_o = l.part_ml + round_up(pairs * 2 * 128 * 2 * 2 * sizeof(float), 256);
+    l.total = l.part_o + pairs * 2 * 128 * (size_t)d->d_c * 2;
+    return l;
+}
+
+// Bytes at the workspace start that every call zeroes first: the status word,
+// and the balanced plan's merge counters.
+size_t plan_zero_bytes(const mla_dims *d, const DecodePlan &pl) {
+    return pl.persist_groups > 0 ? persist_layout(d, pl).prefix : sizeof(int);
+}
+
 size_t plan_workspace_bytes(const mla_dims *d, const DecodePlan &pl) {
+    if (pl.persist_groups > 0) return persist_layout(d, pl).total;
     if (pl.b_tail == 0) return attn_workspace_bytes(d, pl.splits) + order_bytes(d, pl);
     mla_dims t = *d;
     t.B = pl.b_tail;
@@ -235,6 +303,18 @@ void set_partials(mla::AttnParams &p, const mla_dims *d, int nb, int splits, voi
 // leave the SMs, and only they are merged.
 cudaError_t launch_decode_plan(const mla_dims *d, const DecodePlan &pl, mla::AttnParams p, void *workspace,
                                cudaStream_t st) {
+    if (pl.persist_groups > 0) {
+        const PersistLayout l = persist_layout(d, pl);
+        char *base = (char *)workspace;
+        p.counters = (int *)(base + l.counters);
+        p.prefix = (int *)(base + l.prefix);
+        p.ml = (float *)(base + l.ml);
+        p.part_ml = (float *)(base + l.part_ml);
+        p.part_acc = (float *)(base + l.part_o);
+        p.num_splits = 1;
+        p.persist_groups = pl.persist_groups;
+        return mla::launch_attn_persist(p, st);
+    }
     const size_t ob = order_bytes(d, pl);
     if (pl.lpt) {
         p.lpt = 1;
@@ -351,12 +431,14 @@ MLA_API int mla_absorb_q(const mla_dims *dims, const void *q_nope, const void *q
 MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache) {
     if (check_dims(dims) || check_cache(dims, cache)) return 0;
     const DecodePlan pl = plan_decode(dims, cache, 0);
+    if (pl.persist_groups > 0) return pl.persist_groups;
     return pl.b_tail ? pl.tail_splits : pl.splits;
 }
 
 MLA_API size_t mla_decode_workspace_size(const mla_dims *dims, const mla_cache *cache, int num_splits) {
     if (check_dims(dims) || check_cache(dims, cache)) return 0;
-    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+    if (num_splits < MLA_SPLITS_BALANCED || num_splits > kMaxSplits) return 0;
+    if (num_splits == MLA_SPLITS_BALANCED && !balanced_supported(dims, cache)) return 0;
     return plan_workspace_bytes(dims, plan_decode(dims, cache, num_splits));
 }
 
@@ -366,7 +448,8 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
     if (s) return s;
     if (!cache) return MLA_ERR_NULL;
     if ((s = check_cache(dims, cache))) return s;
-    if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (num_splits < MLA_SPLITS_BALANCED || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (num_splits == MLA_SPLITS_BALANCED && !balanced_supported(dims, cache)) return MLA_ERR_UNSUPPORTED;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     const DecodePlan pl = plan_decode(dims, cache, num_splits);
@@ -376,7 +459,7 @@ MLA_API int mla_decode_attn(const mla_dims *dims, const void *q_cat, const mla_c
         if (!aligned16(q_cat) || !aligned16(o_lat) || !aligned16(lse)) return MLA_ERR_ALIGN;
     }
     cudaStream_t st = as_stream(stream);
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, plan_zero_bytes(dims, pl), st) != cudaSuccess) return MLA_ERR_CUDA;
     if (dims->B == 0) return MLA_OK;
 
     mla::AttnParams p = make_params(dims, cache);
@@ -591,7 +674,8 @@ MLA_API int mla_decode_step(const mla_dims *dims, const void *q_nope, const void
     if (s) return s;
     if (!cache) return MLA_ERR_NULL;
     if ((s = check_cache(dims, cache))) return s;
-    if (num_splits < 0 || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (num_splits < MLA_SPLITS_BALANCED || num_splits > kMaxSplits) return MLA_ERR_SHAPE;
+    if (num_splits == MLA_SPLITS_BALANCED && !balanced_supported(dims, cache)) return MLA_ERR_UNSUPPORTED;
     if (!workspace) return MLA_ERR_NULL;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     const DecodePlan pl = plan_decode(dims, cache, num_splits);
@@ -607,7 +691,7 @@ MLA_API int mla_decode_step(const mla_dims *dims, const void *q_nope, const void
     // the status reset comes first, so that nothing but kernels separates the three
     // launches: the attention and out_proj grids are launched programmatically and
     // start while their predecessor runs, reading its output only once it completed
-    if (cudaMemsetAsync(workspace, 0, sizeof(int), st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, plan_zero_bytes(dims, pl), st) != cudaSuccess) return MLA_ERR_CUDA;
     if (dims->B == 0) return MLA_OK;
     cudaError_t e = mla::launch_absorb_q_tc(*dims, q_nope, q_rope, w_uk, q_cat, st, true);
     if (e != cudaSuccess) return MLA_ERR_CUDA;

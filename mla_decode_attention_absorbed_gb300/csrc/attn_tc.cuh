@@ -87,6 +87,18 @@ struct Smem {
     int lpt_b, lpt_L;  // longest-first order: the sequence of this CTA's work item, its length
     int armed;    // last tile whose receive the exchange warp armed
     int received; // last tile the softmax warps received
+    // persistent kernel only (attn_persist.cu): one phase per work item with tiles
+    uint64_t q_next;       // the epilogue warps loaded the next item's queries
+    uint64_t s_last;       // the item's last score chain completed
+    uint64_t o_last;       // the item's last P . V completed
+    uint64_t o_free;       // the epilogue warps drained the item's O
+    uint64_t ml_ready[2];  // by item parity: the softmax warps left the item's (m, l)
+    uint64_t merge_full;   // the pieces' rows a merge step needs landed in the ring
+    int walk_b;            // the sequence holding the first tile of this pair's range
+    int n_pending;         // merges this CTA owes (it wrote the sequence's last piece): at most 2
+    int pend_b[2];         // their sequences
+    long long walk_S;      // walk_b's first tile in the batch's tile order
+    long long pend_S[2];   // the pending sequences' first tiles
 };
 
 // the whole block, with no realignment slack, within the 227 KB a CTA may use

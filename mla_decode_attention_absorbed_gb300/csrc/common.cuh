@@ -55,7 +55,42 @@ struct AttnParams {
     // out records MLA_ERR_TIMEOUT and the CTA unwinds (the waits that drain copies
     // and MMAs still in flight keep the default)
     unsigned long long wait_ns;
+    // persistent decode (attn_persist.cu): persist_groups x (128-row blocks) CTA
+    // pairs, each group an equal contiguous range of the batch's sequence tiles
+    // (in batch order); a sequence one range holds whole is written out directly,
+    // the others leave normalised bf16 pieces in part_acc ([pair][2 slots][128
+    // rows][d_c]) with their (m, l) in part_ml, and the CTA that writes a
+    // sequence's last piece merges them (counters: [B][row blocks][2 CTAs],
+    // zeroed with the status word).  prefix: the batch's tile prefix (B + 1 ints);
+    // ml: the (m, l) the softmax warps hand to the epilogue warps.
+    int persist_groups;
+    int *counters;
+    int *prefix;
+    float *ml;
 };
+
+// Persistent decode: groups of CTA pairs in use for T sequence tiles (at most
+// max_groups, each range at least kMinGroupTiles tiles long), group g's range
+// [group_first_tile(g), group_first_tile(g + 1)) of the tiles, the group whose
+// range holds tile t, and the partial slot a sequence starting at tile S takes
+// in group g (0: it began at or before the range, the group's first item; 1: it
+// began inside and runs past it, the group's last item).
+constexpr int kMinGroupTiles = 8;
+__host__ __device__ __forceinline__ int persist_groups(int max_groups, long long T) {
+    long long g = T / kMinGroupTiles;
+    if (g > max_groups) g = max_groups;
+    return g < 1 ? 1 : (int)g;
+}
+__host__ __device__ __forceinline__ long long group_first_tile(int g, int G, long long T) { return (long long)g * T / G; }
+__host__ __device__ __forceinline__ int group_of_tile(long long t, int G, long long T) {
+    int g = (int)((t * G) / T);
+    while (g + 1 < G && group_first_tile(g + 1, G, T) <= t) ++g;
+    while (g > 0 && group_first_tile(g, G, T) > t) --g;
+    return g;
+}
+__host__ __device__ __forceinline__ int persist_slot(long long S, int g, int G, long long T) {
+    return S <= group_first_tile(g, G, T) ? 0 : 1;
+}
 
 // Record the first device-side error; later ones keep the first.
 __device__ __forceinline__ void set_status(int *status, int code) {

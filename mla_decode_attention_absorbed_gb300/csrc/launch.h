@@ -30,6 +30,7 @@ inline AppendPlan append_plan(int M, int d_c, int d_model) {
 cudaError_t launch_cache_append_tc(const AttnParams &p, int d_model, const void *x, const void *w_dkv,
                                    const void *k_rope, float *part, cudaStream_t st);
 cudaError_t launch_attn_tc(const AttnParams &p, cudaStream_t st);
+cudaError_t launch_attn_persist(const AttnParams &p, cudaStream_t st);
 cudaError_t launch_attn_expand(const AttnParams &p, cudaStream_t st);
 // Expanded rows [V_h | K_h | k_rope] of every cached token < seq_lens[b] of every
 // sequence and head (the prefill "expand" form), into exp [B][H][capacity][W_e].

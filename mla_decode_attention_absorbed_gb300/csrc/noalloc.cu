@@ -40,7 +40,7 @@ extern "C" {
 MLA_API int mla_decode_attn_noalloc(const mla_dims *dims, const void *q_cat, const mla_cache *cache, void *o_lat,
                                     float *lse, int num_splits, int *device_status, void *stream) {
     if (!dims || !cache) return MLA_ERR_NULL;
-    if (num_splits < 0) return MLA_ERR_SHAPE;
+    if (num_splits < MLA_SPLITS_BALANCED) return MLA_ERR_SHAPE;
     if (device_status && ((uintptr_t)device_status & 3u)) return MLA_ERR_ALIGN;
     // The library's plan keeps its split partials to about one wave of work items
     // (about 20 MB at most), so it fits the array; a plan or an explicit split

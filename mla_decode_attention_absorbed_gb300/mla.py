@@ -38,6 +38,7 @@ class Cache(ctypes.Structure):
 
 KV_BF16, KV_E4M3 = 0, 1
 ABI_VERSION = 2
+SPLITS_BALANCED = -1  # num_splits asking for the balanced plan (MLA_SPLITS_BALANCED)
 
 
 EXPORTS = ("mla_status_string", "mla_abi_version", "mla_absorb_q", "mla_decode_workspace_size",

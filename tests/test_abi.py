@@ -95,7 +95,7 @@ def test_workspace_and_split_queries(lib):
     for paged in (False, True):
         c = fake_cache(4096, paged)
         s = lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c))
-        assert 1 <= s <= 64
+        assert 1 <= s <= 152
         one = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 1)
         four = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 4)
         assert one >= 4 and four >= 64 * 4 * 128 * 512 * 4
@@ -104,32 +104,98 @@ def test_workspace_and_split_queries(lib):
     assert naive >= 64 * 128 * 4096 * 256 * 2
 
 
+def one_cta(B, s_q):
+    """Dims whose attention runs one CTA per 128-row work item (d_c <= 256)."""
+    return mla.Problem(B, 128, s_q, 256, 64, 128, 128, 0.1)
+
+
 def test_tail_plan_fills_the_last_wave(lib):
-    """More 128-row work items than a wave of 76 clusters holds: the plan leaves
-    them whole except the sequences of the partly filled last wave, which it
+    """One-CTA dims, more 128-row work items than a wave of 152 SMs holds: the plan
+    leaves them whole except the sequences of the partly filled last wave, which it
     splits, and the workspace holds only their partials."""
-    d = dsv3(B=64, s_q=4).dims()  # 256 work items = 3 waves + 28
+    d = one_cta(B=40, s_q=4).dims()  # 160 work items = 1 wave + 8 (2 sequences)
     c = fake_cache(8192)
-    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 2  # 76 // 28
-    tail_rows = 7 * 2 * 4 * 128  # the last 7 sequences, 2 pieces, 512 rows each
+    # 152 // 8 = 19 pieces, capped at 16 (pieces of at least 8 of the 128 tiles)
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 16
+    tail_rows = 2 * 16 * 4 * 128  # the last 2 sequences, 16 pieces, 512 rows each
     need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 0)
-    assert tail_rows * 512 * 4 <= need < 2 * tail_rows * 512 * 4
+    assert tail_rows * 256 * 4 <= need < 2 * tail_rows * 256 * 4
     # an explicit count splits every sequence
-    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 2) >= 64 * 2 * 512 * 512 * 4
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 2) >= 40 * 2 * 512 * 256 * 4
     # whole waves, or one wave, keep the plain plan
-    d = dsv3(B=76, s_q=1).dims()
+    d = one_cta(B=38, s_q=4).dims()
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
     assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 0) < 4096
-    d = dsv3(B=64, s_q=1).dims()
+    d = one_cta(B=30, s_q=4).dims()
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
     # pieces stay at least 8 tiles long: a 1024-token history allows 2 pieces
-    d = dsv3(B=20, s_q=4).dims()  # 80 work items: one sequence in the last wave
+    d = one_cta(B=39, s_q=4).dims()  # 156 work items: one sequence in the last wave
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(fake_cache(1024))) == 2
     # the tail's pieces must still fit the grid: 65,535 sequences leave no room for them
-    d = dsv3(B=65535, s_q=1).dims()  # 65,535 items = 862 waves + 23
+    d = one_cta(B=65535, s_q=1).dims()  # 65,535 items = 431 waves + 23
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
-    d = dsv3(B=65535 - 76, s_q=1).dims()  # 65,459 items = 861 waves + 23: 23 x 3 pieces fit
-    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 3
+    d = one_cta(B=65535 - 152, s_q=1).dims()  # 65,383 items = 430 waves + 23: 23 x 6 pieces fit
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 6
+
+
+def test_balanced_plan_for_pair_kernels(lib):
+    """DeepSeek-V3 widths (CTA pairs), MLA_SPLITS_BALANCED: the batch's tiles are
+    dealt out to groups of pairs, one group per 76 // (128-row blocks) pair slots,
+    capped so that a range holds at least 8 tiles of what max_seq_len allows; the
+    workspace holds the merge counters, the tile prefix, the (m, l) hand-over and
+    two bf16 pieces per pair.  The library's choice takes it only in one wave of
+    work items and where it gives a pair at least 16 tiles fewer than the split
+    plan; FP8 caches, one-CTA widths and 4096 sequences or more cannot have it."""
+    def rup(n):
+        return (n + 255) // 256 * 256
+
+    def balanced_bytes(B, pairs, n_rb, d_c=512):
+        # status, merge counters, tile prefix, (m, l) hand-over, pieces' (m, l), pieces' rows
+        return (256 + rup(B * n_rb * 2 * 4) + rup((B + 1) * 4) + rup(pairs * 2 * 2 * 128 * 3 * 4)
+                + rup(pairs * 2 * 128 * 16) + pairs * 2 * 128 * d_c * 2)
+
+    BAL = mla.SPLITS_BALANCED
+    c = fake_cache(4096)
+    # (3 sequences x 64 tiles allow 192 / 8 = 24 ranges, fewer than the 76 // 3 = 25 slots)
+    for B, s_q, groups in ((64, 1, 76), (16, 1, 76), (64, 4, 19), (64, 2, 38), (3, 3, 24)):
+        d = dsv3(B=B, s_q=s_q).dims()
+        need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), BAL)
+        assert need == balanced_bytes(B, groups * s_q, s_q), (B, s_q)
+    # few tiles: 2 sequences of at most 256 tokens (8 tiles) make one range
+    d = dsv3(B=2, s_q=1).dims()
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(fake_cache(256)), BAL) == balanced_bytes(2, 1, 1)
+    # the library's choice: 64 x 4096 tokens, one sequence a pair (64 tiles) against
+    # 54 balanced: the unsplit plan
+    d = dsv3(B=64, s_q=1).dims()
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 1
+    # 16 x 32768 tokens: 4 pieces of 128 tiles against 108 balanced: the balanced plan
+    d = dsv3(B=16, s_q=1).dims()
+    c32 = fake_cache(32768)
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c32)) == 76
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c32), 0) == balanced_bytes(16, 76, 1)
+    # 16 x 4096 tokens: 16 tiles a piece against 14: the split plan
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 4
+    # more work items than a wave of 76 pairs: the tail plan (256 items = 3 waves + 28)
+    d = dsv3(B=64, s_q=4).dims()
+    c8 = fake_cache(8192)
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c8)) == 2  # 76 // 28
+    tail_rows = 7 * 2 * 4 * 128  # the last 7 sequences, 2 pieces, 512 rows each
+    need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c8), 0)
+    assert tail_rows * 512 * 4 <= need < 2 * tail_rows * 512 * 4
+    # an explicit count keeps the split plan
+    d = dsv3(B=64, s_q=1).dims()
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 2) >= 64 * 2 * 128 * 512 * 4
+    # not available: 4096 sequences, an FP8 cache, one-CTA widths; below -1 is no count
+    nul = ctypes.c_void_p(0)
+    a = ctypes.c_void_p(0x1000)
+    fp8 = mla.Cache(0x10000, 4096 * 576, 4096, None, 0, 64, 0, 0x20000, 0, 1, 0.5)
+    for dd, cc in ((dsv3(B=4096, s_q=1).dims(), c), (dsv3(B=64, s_q=1).dims(), fp8), (one_cta(8, 1).dims(), c)):
+        assert lib.mla_decode_workspace_size(ctypes.byref(dd), ctypes.byref(cc), BAL) == 0
+        assert lib.mla_decode_attn(ctypes.byref(dd), a, ctypes.byref(cc), a, a, a, 1 << 30, BAL, nul) == 6
+    d = dsv3(B=64, s_q=1).dims()
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), -2) == 0
+    assert lib.mla_decode_attn(ctypes.byref(d), a, ctypes.byref(c), a, a, a, 1 << 30, -2, nul) == 2
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(fp8)) == 1  # one wave of 64 pairs
 
 
 def test_expand_path_grid_limit(lib):
@@ -179,7 +245,8 @@ NOALLOC_BYTES = 32 << 20  # the no-allocation entry point's array
 def test_library_plan_fits_the_noalloc_array(lib):
     """mla_decode_attn_noalloc runs the library's own plan (num_splits 0) in a fixed
     32 MiB array: over the supported envelope that plan's workspace never exceeds it
-    (split partials stay near one wave of 128-row work items)."""
+    (split partials stay near one wave of 128-row work items), nor does the
+    balanced plan's (two bf16 pieces per pair slot)."""
     worst = 0
     for d_c, d_rope in ((64, 16), (256, 64), (320, 16), (512, 64)):
         for H, s_q in ((16, 1), (128, 1), (128, 2), (128, 4), (64, 3), (1, 1), (512, 128)):
@@ -194,5 +261,8 @@ def test_library_plan_fits_the_noalloc_array(lib):
                         if not paged:
                             c = mla.Cache(0x10000, T * (d_c + d_rope), T, None, 0, 64, 0, 0x20000, 0)
                         n = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 0)
+                        worst = max(worst, n)
+                        # the balanced plan, where the dims allow it, fits as well
+                        n = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), mla.SPLITS_BALANCED)
                         worst = max(worst, n)
     assert 0 < worst <= NOALLOC_BYTES, worst

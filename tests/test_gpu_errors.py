@@ -21,7 +21,7 @@ def _lib():
     mla.load()
 
 
-@pytest.mark.parametrize("splits", [1, 3])
+@pytest.mark.parametrize("splits", [mla.SPLITS_BALANCED, 0, 1, 3])  # balanced: its merge writes them
 def test_bad_lengths_flagged(splits):
     cfg = MLAConfig("bl", B=4, s_q=2, T=200, **DSV3_DIMS)
     inp = make_inputs(cfg, seq_lens=[150, 1, 200, 0])  # 1 < s_q and 0 are invalid

@@ -16,6 +16,9 @@ from helpers import check_against_oracle, gpu_cache, run_gpu, sample_rows, to_de
 pytestmark = pytest.mark.gpu
 
 DSV3_DIMS = dict(H=128, d_c=512, d_rope=64, d_nope=128, d_v=128)
+# widths whose attention runs one CTA per 128-row work item (the tail and
+# longest-first plans are theirs; the pair kernels take the balanced plan)
+ONE_CTA_DIMS = dict(H=128, d_c=256, d_rope=64, d_nope=128, d_v=128)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -156,12 +159,12 @@ def test_full_size_sampled(name):
 
 
 def test_tail_plan_matches_unsplit_and_oracle():
-    """80 work items on 76 cluster slots: the last sequence runs in two pieces (the
-    grid's last work items, merged), the others unsplit; the result agrees with
-    the unsplit launch and the oracle, and the fused step with the same plan is
-    bit-identical."""
+    """156 work items on 152 SM slots (one CTA per item): the last sequence runs in
+    two pieces (the grid's last work items, merged), the others unsplit; the result
+    agrees with the unsplit launch and the oracle, and the fused step with the same
+    plan is bit-identical."""
     from helpers import sample_rows
-    cfg = MLAConfig("tail", B=20, s_q=4, T=1024, seed=61, **DSV3_DIMS)
+    cfg = MLAConfig("tail", B=39, s_q=4, T=1024, seed=61, **ONE_CTA_DIMS)
     inp = make_inputs(cfg)
     d = to_dev(inp)
     prob, cache = gpu_cache(cfg, d)
@@ -187,12 +190,13 @@ def test_tail_plan_matches_unsplit_and_oracle():
 
 
 def test_longest_first_order_ragged():
-    """100 ragged sequences on 76 cluster slots: the work order is longest first
-    (ranked on the device) and the 24 shortest sequences, the last wave, run in 3
-    pieces each; whole sequences match the explicit unsplit launch bit for bit,
-    everything matches the oracle, and the fused step is bit-identical."""
+    """200 ragged sequences on 152 SM slots (one CTA per item): the work order is
+    longest first (ranked on the device) and the 48 shortest sequences, the last
+    wave, run in 3 pieces each; whole sequences match the explicit unsplit launch
+    bit for bit, everything matches the oracle, and the fused step is
+    bit-identical."""
     from helpers import sample_rows
-    cfg = MLAConfig("lpt", B=100, s_q=1, len_lo=64, len_hi=2048, paged=True, seed=62, **DSV3_DIMS)
+    cfg = MLAConfig("lpt", B=200, s_q=1, len_lo=64, len_hi=2048, paged=True, seed=62, **ONE_CTA_DIMS)
     inp = make_inputs(cfg)
     d = to_dev(inp)
     prob, cache = gpu_cache(cfg, d)
@@ -204,9 +208,9 @@ def test_longest_first_order_ragged():
     lens = inp["seq_lens"].tolist()
     order = sorted(range(cfg.B), key=lambda b: (-lens[b], b))
     rows = cfg.s_q * cfg.H
-    for b in order[:76]:  # whole sequences
+    for b in order[:152]:  # whole sequences
         assert torch.equal(auto["o_lat"].view(cfg.B, -1)[b], one["o_lat"].view(cfg.B, -1)[b]), b
-    split_rows = [b * rows + r for b in order[76:] for r in (0, rows - 1)]
+    split_rows = [b * rows + r for b in order[152:] for r in (0, rows - 1)]
     check_against_oracle(cfg, inp, auto, rows=sorted(set(sample_rows(cfg, 16) + split_rows)))
     dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], cfg.page_size)
     out_f = dec.step(d["q_nope"], d["q_rope"]).clone()
@@ -216,6 +220,64 @@ def test_longest_first_order_ragged():
     assert mla.read_status(dec.workspace) == 0
     assert torch.equal(out_f, out_s) and torch.equal(lse_f, dec.lse)
     assert torch.equal(lse_f.cpu(), auto["lse"])
+
+
+# ---------------------------------------------------------------- balanced plan (pair kernels)
+def _balanced_case(cfg, inp, rows=None):
+    """The balanced plan (MLA_SPLITS_BALANCED) against the explicit unsplit launch
+    and the oracle; the fused step with the same plan is bit-identical to separate
+    calls."""
+    d = to_dev(inp)
+    prob, cache = gpu_cache(cfg, d)
+    auto = run_gpu(cfg, inp, num_splits=mla.SPLITS_BALANCED)
+    one = run_gpu(cfg, inp, num_splits=1)
+    assert auto["status"] == 0 and one["status"] == 0
+    within_tolerance(auto["o_lat"].double(), one["o_lat"].double(), "balanced vs unsplit o_lat")
+    within_tolerance(auto["lse"].double(), one["lse"].double(), "balanced vs unsplit lse", rel=1e-3, abs_=1e-3)
+    check_against_oracle(cfg, inp, auto, rows=rows)
+    dec = mla.Decoder(prob, d["kv"], d["seq_lens"], d["w_uk"], d["w_uv"], d["block_table"], cfg.page_size,
+                      num_splits=mla.SPLITS_BALANCED)
+    out_f = dec.step(d["q_nope"], d["q_rope"]).clone()
+    lse_f = dec.lse.clone()
+    out_s = dec(d["q_nope"], d["q_rope"]).clone()
+    torch.cuda.synchronize()
+    assert mla.read_status(dec.workspace) == 0
+    assert torch.equal(out_f, out_s) and torch.equal(lse_f, dec.lse)
+    assert torch.equal(lse_f.cpu(), auto["lse"])
+    return prob, cache
+
+
+def test_balanced_plan_ragged_paged():
+    """Ragged paged sequences, two query tokens (two row blocks, 38 groups): ranges
+    start and end inside sequences, so pieces of most sequences merge."""
+    cfg = MLAConfig("bal", B=9, s_q=2, len_lo=1, len_hi=3000, paged=True, seed=71, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    _balanced_case(cfg, inp, rows=sample_rows(cfg, 64))
+
+
+def test_balanced_plan_one_long_sequence():
+    """One 8,257-token sequence (130 tiles) dealt out to 16 ranges of about 8 tiles."""
+    cfg = MLAConfig("bal1", B=1, s_q=1, T=8257, seed=72, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    _balanced_case(cfg, inp)
+
+
+def test_balanced_plan_many_short_sequences():
+    """300 short sequences: each range holds many whole sequences (written out
+    directly) between the pieces at its two ends."""
+    cfg = MLAConfig("bal2", B=300, s_q=1, len_lo=1, len_hi=300, seed=73, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    _balanced_case(cfg, inp, rows=sample_rows(cfg, 64) + [128 * b for b in range(0, 300, 7)])
+
+
+def test_balanced_plan_empty_causal_piece():
+    """Two ranges of 20 tiles; the second starts at the first sequence's last tile,
+    which holds tokens 640 and 641 only: with four query tokens the first two row
+    blocks (queries 0 and 1, limits 638 and 639) see nothing of it, so their piece
+    is empty and must merge as nothing."""
+    cfg = MLAConfig("bal3", B=2, s_q=4, T=642, seed=74, **DSV3_DIMS)
+    inp = make_inputs(cfg, seq_lens=[642, 576])
+    _balanced_case(cfg, inp)
 
 
 # ---------------------------------------------------------------- naive comparison path
