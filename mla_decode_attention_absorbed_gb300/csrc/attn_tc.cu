@@ -410,6 +410,9 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         } else if (warp == kProducerWarp) {
             // ------------------------------------------------------------ TMA producer, dense
             if (lane == 0) {
+                // every cache line is read once: it leaves L2 first, ahead of the
+                // queries and outputs the projections around this kernel reuse
+                const uint64_t pol = l2_evict_first();
                 // y / z coordinates of tile n's box, or false if its page is outside the pool
                 auto coords = [&](int n, int &y, int &z) -> bool {
                     const int tok = t0 + n * kTile;
@@ -452,14 +455,14 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         mbar_arrive_expect_tx(&sm.landed[s], g.nbox * 4096);
                         for (int bx = 0; bx < g.nbox; ++bx) {
                             uint8_t *raw = sm.kv[s] + bx * kBoxBytes + 4096;
-                            if (kPaged) tma_load_2d(raw, tm, &sm.landed[s], g.x_u32 + 16 * bx, y);
-                            else tma_load_3d(raw, tm, &sm.landed[s], g.x_u32 + 16 * bx, y, z);
+                            if (kPaged) tma_load_2d_hint(raw, tm, &sm.landed[s], g.x_u32 + 16 * bx, y, pol);
+                            else tma_load_3d_hint(raw, tm, &sm.landed[s], g.x_u32 + 16 * bx, y, z, pol);
                         }
                     } else {
                         mbar_arrive_expect_tx(&sm.full[s], g.nbox * kBoxBytes);
                         for (int bx = 0; bx < g.nbox; ++bx) {
-                            if (kPaged) tma_load_2d(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y);
-                            else tma_load_3d(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y, z);
+                            if (kPaged) tma_load_2d_hint(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y, pol);
+                            else tma_load_3d_hint(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y, z, pol);
                         }
                     }
                     issued = n + 1;
