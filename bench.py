@@ -557,7 +557,8 @@ def main_ours(args):
     value = total_flops / (ms * 1e-3) / 1e12
     roof = roofline_of(w, r["attn_ms"], pk)
     roof["traffic"] = traffic_for(f"attn{'_fp8' if args.kv == 'fp8' else ''}:{cfg.name}")
-    roof["kernel"] = "mla_decode_attn (split-T attention + LSE combine)" + (
+    roof["kernel"] = ("mla_decode_attn, balanced plan (persistent pair kernel, in-launch merge)" if "balanced" in r["plan"]
+                      else "mla_decode_attn (split-T attention + LSE combine)") + (
         ", FP8 E4M3 cache dequantised on chip, fp16 MMAs" if args.kv == "fp8" else "")
     roof["kernel_timing"] = (f"CUDA events around each of {args.steps} replays of the attention call captured "
                              "as a CUDA graph (no host launch work inside)")
