@@ -626,24 +626,27 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         has_nx = true;
                         break;
                     }
+                // A wait that runs out fails this warp's item (nothing more of it is
+                // done); the four warps agree below and leave together, so that none is
+                // left at a barrier the others have passed.
+                bool fail = false;
                 if (has_nx) {  // the next item's queries, once this item's last score chain has run
                     q_fetch(nx.b, 0);
-                    if (!warp_wait(sm, &sm.s_last, k & 1)) {
-                        raise_abort<true>(sm, p, peer);
-                        ok = false;
-                        break;
+                    fail = !warp_wait(sm, &sm.s_last, k & 1);
+                    if (!fail) {
+                        tc_fence_after();
+                        q_put(0);
+                        for (int c0 = kQRound; c0 < g.sw; c0 += kQRound) {
+                            q_fetch(nx.b, c0);
+                            q_put(c0);
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(&sm.q_next);
                     }
-                    tc_fence_after();
-                    q_put(0);
-                    for (int c0 = kQRound; c0 < g.sw; c0 += kQRound) {
-                        q_fetch(nx.b, c0);
-                        q_put(c0);
-                    }
-                    tmem_st_wait();
-                    tc_fence_before();
-                    mbar_arrive(&sm.q_next);
                 }
-                if (!warp_wait(sm, &sm.o_last, k & 1) || !warp_wait(sm, &sm.ml_ready[k & 1], (k >> 1) & 1)) {
+                fail = fail || !warp_wait(sm, &sm.o_last, k & 1) || !warp_wait(sm, &sm.ml_ready[k & 1], (k >> 1) & 1);
+                if (named_bar_or(kBarEpi, 128, fail)) {
                     raise_abort<true>(sm, p, peer);
                     ok = false;
                     break;

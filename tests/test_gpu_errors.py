@@ -119,3 +119,26 @@ def test_wait_timeout_reported_and_recovered():
     g = run_gpu(cfg, inp)
     assert g["status"] == 0
     check_against_oracle(cfg, inp, g)
+
+
+def test_wait_timeout_balanced_plan():
+    """The same on the balanced plan's persistent pair kernel (DeepSeek-V3 widths,
+    three sequences cut between tile ranges): waits give up in every role, the
+    epilogue warps agree before leaving their item loop (none is left at a barrier
+    the others passed), the pair meets at its closing cluster barrier, and the next
+    call, with the default bound, runs clean and matches the oracle."""
+    cfg = MLAConfig("to_bal", B=3, s_q=1, T=1500, seed=31, **DSV3_DIMS)
+    inp = make_inputs(cfg)
+    d = to_dev(inp)
+    prob, cache = gpu_cache(cfg, d)
+    q_cat = mla.absorb_q(prob, d["q_nope"], d["q_rope"], d["w_uk"])
+    try:
+        mla.set_wait_limit_ns(1)
+        _, _, ws = mla.decode_attn(prob, q_cat, cache, num_splits=mla.SPLITS_BALANCED)
+        torch.cuda.synchronize()
+        assert mla.read_status(ws) == 8  # MLA_ERR_TIMEOUT
+    finally:
+        mla.set_wait_limit_ns(0)
+    g = run_gpu(cfg, inp, num_splits=mla.SPLITS_BALANCED)
+    assert g["status"] == 0
+    check_against_oracle(cfg, inp, g)
