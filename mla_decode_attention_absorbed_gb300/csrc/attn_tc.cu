@@ -38,8 +38,9 @@
 //  - Sparse lists over a bf16 cache: the listed rows are gathered straight into
 //    the same 4-stage ring by two engines at once -- the producer's
 //    tile::gather4 copies (four rows of one 128-byte box per copy) take the
-//    first two boxes of a row, and four loader warps take the rest with 16-byte
-//    cp.async copies (the tensor-memory-access unit alone moves one 4-row box in
+//    leading boxes of a row, and four loader warps the last two with 16-byte
+//    cp.async copies, on both CTAs of a pair (the one with the RoPE key's fifth
+//    box gathers three) (the tensor-memory-access unit alone moves one 4-row box in
 //    about 70 cycles, too slow for 80 boxes a tile).  Entries that take no part
 //    are gathered from row -1, which the copy engine fills with zeros.
 //  - FP8 caches: the producer copies each tile's row-major E4M3 codes into the
@@ -178,6 +179,10 @@ __device__ __forceinline__ void convert_fp8_rows(uint8_t *box, int r0, unsigned 
     }
 }
 
+// bf16 sparse: 128-byte boxes of a row the producer gathers (tile::gather4);
+// the loader warps copy the last two, so both CTAs of a pair load the same.
+__device__ __forceinline__ int tma_boxes_of(const Geo &g) { return min(g.nbox, max(kTmaBoxes, g.nbox - 2)); }
+
 template <bool kSplit, bool kPaged, bool kSparse, bool kFp8>
 __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
     attn_tc(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1, const AttnParams p,
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
 
     if (threadIdx.x == 0) {
         // the loaders of a CTA whose slice has no box past the gathered ones stay idle
-        const bool loading = kLoaders && g.nbox > kTmaBoxes;
+        const bool loading = kLoaders && g.nbox > tma_boxes_of(g);
         for (int s = 0; s < kRing; ++s) {
             mbar_init(&sm.full[s], kStaged ? kNConv : (loading ? 1 + kConvWarps : 1));
             mbar_init(&sm.empty[s], 1);
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             // block's query may see, 0 <= j <= L - s_q + i (all rows of a block share
             // i), on a page inside the pool.  Lanes 0-15 then gather rows 4q .. 4q+3
             // with tile::gather4: FP8, the whole slice of each row into the raw ring;
-            // bf16, the first kTmaBoxes 128-byte boxes of each row into the operand
+            // bf16, the first tma_boxes_of(g) 128-byte boxes of each row into the operand
             // stage (the loader warps copy the rest).  Entries that take no part are
             // gathered from row -1, which reads as zeros.  The next tile's entries are
             // loaded one tile ahead, so their latency hides behind the wait for a
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             const int lim = L - p.s_q + iq;
             const int *list = p.indices + ((long long)b * p.s_q + iq) * p.topk;
             const long long seq_rows = p.seq_stride / W;  // contiguous: rows between sequences
-            const int nbt = min(g.nbox, kTmaBoxes);
+            const int nbt = kLoaders ? tma_boxes_of(g) : min(g.nbox, kTmaBoxes);
             auto fetch = [&](int n, int (&j)[2]) {
     #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -572,7 +577,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             }
         } else if (warp >= kConvWarp0 && kLoaders) {
             // ------------------------------------------------------------ loaders (bf16 sparse)
-            // Boxes kTmaBoxes .. nbox-1 of every listed row, copied 16 bytes at a time
+            // Boxes tma_boxes_of(g) .. nbox-1 of every listed row, copied 16 bytes at a time
             // with cp.async straight into the swizzled stage (chunk c of row r goes to
             // chunk (c % 8) ^ (r % 8) of row r of box c / 8).  Loader warp lw owns rows
             // 16 lw .. 16 lw + 15 and resolves their entries itself (lanes 0-15, one
@@ -587,7 +592,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             const int lim = L - p.s_q + iq;
             const int *list = p.indices + ((long long)b * p.s_q + iq) * p.topk;
             const long long seq_rows = p.seq_stride / W;
-            const int c0 = 8 * kTmaBoxes;  // first chunk of a row the loaders copy
+            const int c0 = 8 * tma_boxes_of(g);  // first chunk of a row the loaders copy
             const int nl = g.kw / 8 - c0;  // chunks per row they copy (even)
             const __nv_bfloat16 *kvb = static_cast<const __nv_bfloat16 *>(p.kv);
             auto entry = [&](int n) -> int {  // lanes 0-15: list entry of row 16 lw + lane of tile n

@@ -26,7 +26,7 @@ constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
 constexpr int kProducerWarp = 8, kMmaWarp = 9, kExchangeWarp = 10, kSumWarp = 11, kConvWarp0 = 12;
 constexpr int kConvWarps = 4;     // loader warps (bf16 sparse)
 constexpr int kFp8ConvWarps = 4;  // converter warps (FP8)
-constexpr int kTmaBoxes = 2;      // bf16 sparse: boxes of a row gathered by tile::gather4
+constexpr int kTmaBoxes = 2;      // bf16 sparse: boxes of a row gathered by tile::gather4, at least
 
 constexpr int kRing = 4;          // operand-ring stages (tiles in flight into the MMAs)
 
