@@ -51,13 +51,15 @@ struct ProjArgs {
     bool trigger;
 };
 
-// BN = 512 (absorb at d_c = 512: a whole head per CTA, one wave of CTAs) runs two
-// N = 256 MMAs per K step into the two halves of tensor memory, with a 2-stage
-// ring (K = d_nope is two chunks).
-template <int BN>
+// BN = 512 (a whole d_c = 512 head per CTA) would run two N = 256 MMAs per K step
+// into the two halves of tensor memory.  The absorb GEMM (K-major B, K = d_nope:
+// two chunks) at BN = 256 takes a 2-stage ring, so that two CTAs fit an SM: its
+// 2 x H CTAs at d_c = 512 run in one wave (measured against one CTA a head: the
+// dsv3 step 116.4 -> 114.6 us).
+template <int BN, bool kBMN>
 struct ProjSmem {
     static constexpr uint32_t kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : BN <= 256 ? 256 : 512;
-    static constexpr int kStagesN = BN > 256 ? 2 : kStages;
+    static constexpr int kStagesN = (BN > 256 || (!kBMN && BN == 256)) ? 2 : kStages;
     static constexpr int kHalves = BN > 256 ? 2 : 1;   // MMAs of N = BN / kHalves per K step
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KB
     static constexpr int kBBytes = BN * kBK * 2;   // 32 KB at BN = 256
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment: the 128-byte swizzle pattern repeats every 8 rows of 128 B
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    using L = ProjSmem<BN>;
+    using L = ProjSmem<BN, kBMN>;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::kStagesN * L::kStageBytes);
     uint64_t *empty = full + L::kStagesN;
     uint64_t *acc_full = empty + L::kStagesN;
@@ -263,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, bool kBMN>
 cudaError_t launch_proj(const CUtensorMap &tA, const CUtensorMap &tB, const ProjArgs &g, cudaStream_t st) {
-    const int smem = ProjSmem<BN>::kBytes;
+    const int smem = ProjSmem<BN, kBMN>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(proj_gemm_tc<BN, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -296,7 +298,7 @@ cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void
     CUtensorMap tA, tB;
     if (!map_rows(&tA, q_nope, M, d.H, d.d_nope)) return cudaErrorInvalidValue;
     // W_UK [H][d_c][d_nope]: K-major B, box 64 (k) x BN (n) x 1
-    const int BN = d.d_c == 512 ? 512 : d.d_c >= 256 ? 256 : d.d_c;  // d_c is a multiple of 64
+    const int BN = d.d_c >= 256 ? 256 : d.d_c;  // d_c is a multiple of 64: N tiles of 256 (two CTAs an SM)
     uint64_t dims[3] = {(uint64_t)d.d_nope, (uint64_t)d.d_c, (uint64_t)d.H};
     uint64_t strides[2] = {(uint64_t)d.d_nope * 2, (uint64_t)d.d_c * d.d_nope * 2};
     uint32_t box[3] = {64, (uint32_t)(BN > 256 ? 256 : BN), 1};
@@ -304,7 +306,6 @@ cudaError_t launch_absorb_q_tc(const mla_dims &d, const void *q_nope, const void
     ProjArgs g{M, d.H, d.d_c, d.d_nope, (__nv_bfloat16 *)q_cat, d.d_c + d.d_rope,
                d.d_rope ? (const __nv_bfloat16 *)q_rope : nullptr, d.d_rope, nullptr, 0, 1, false, trigger};
     switch (BN) {
-        case 512: return launch_proj<512, false>(tA, tB, g, st);
         case 256: return launch_proj<256, false>(tA, tB, g, st);
         case 192: return launch_proj<192, false>(tA, tB, g, st);
         case 128: return launch_proj<128, false>(tA, tB, g, st);
