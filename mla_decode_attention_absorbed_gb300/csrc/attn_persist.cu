@@ -390,6 +390,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             PWalk w = walk0;
             PItem it;
             int n = 0;
+            int next_page = 0;  // paged: the block-table entry of the item's next tile
             while (go && next_item(w, it)) {
                 for (int i = 0; i < it.ntiles; ++i, ++n) {
                     const int s = n % kRing;
@@ -406,16 +407,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         go = false;
                         break;
                     }
-                    const int tok = it.t0 + i * kTile;
+                    // this tile's page id was looked up while the loop waited for its stage
                     int y, z;
                     bool page_ok = true;
                     if (kPaged) {
-                        const int page = __ldg(p.block_table + (long long)it.b * p.max_pages + tok / p.page_size);
+                        const int tok = it.t0 + i * kTile;
+                        const int page = i == 0 ? __ldg(p.block_table + (long long)it.b * p.max_pages + tok / p.page_size)
+                                                : next_page;
                         page_ok = page >= 0 && page < p.num_pages;
                         y = page * p.page_size + tok % p.page_size;
                         z = 0;
                     } else {
-                        y = tok;
+                        y = it.t0 + i * kTile;
                         z = it.b;
                     }
                     if (!page_ok) {
@@ -428,6 +431,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         else tma_load_3d_hint(sm.kv[s] + bx * kBoxBytes, tm, &sm.full[s], g.k0 + 64 * bx, y, z, pol_stream);
                     }
                     issued = n + 1;
+                    if (kPaged && i + 1 < it.ntiles)
+                        next_page = __ldg(p.block_table + (long long)it.b * p.max_pages + (it.t0 + (i + 1) * kTile) / p.page_size);
                     // eight tiles before an item ends, the next item's queries go to L2 for
                     // the epilogue warps that load them at the hand-over
                     if (i == max(0, it.ntiles - 8)) {
@@ -826,9 +831,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int j = 0; j < kHalf; ++j) sc[j] = s0[j];
             }
+            // paged: the block-table entry of the current tile, loaded one tile ahead
+            int page_cur = kPaged ? __ldg(p.block_table + (long long)it.b * p.max_pages + it.t0 / p.page_size) : 0;
             for (int i = 0; i < it.ntiles; ++i, ++n) {
                 float sn[kHalf];
                 const bool more = i + 1 < it.ntiles;
+                const int page_n = page_cur;
+                if (kPaged && more)
+                    page_cur = __ldg(p.block_table + (long long)it.b * p.max_pages + (it.t0 + (i + 1) * kTile) / p.page_size);
                 if (more) {
                     if (!warp_wait(sm, &sm.s_full, (n + 1) & 1)) raise_abort<true>(sm, p, peer);
                     tc_fence_after();
@@ -860,10 +870,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 // mask (only tiles that reach past a limit) and half-row maximum
                 const int tok0 = it.t0 + i * kTile;
                 bool tile_ok = true;
-                if (kPaged) {
-                    const int page = __ldg(p.block_table + (long long)it.b * p.max_pages + tok0 / p.page_size);
-                    tile_ok = page >= 0 && page < p.num_pages;
-                }
+                if (kPaged) tile_ok = page_n >= 0 && page_n < p.num_pages;
                 const bool whole = tile_ok && tok0 + kTile <= it.t1 && tok0 + kTile - 1 <= L - p.s_q + q_first;
                 float mx0 = -INFINITY, mx1 = -INFINITY;
                 if (whole) {

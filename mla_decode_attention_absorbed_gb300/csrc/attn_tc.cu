@@ -432,6 +432,10 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                     return true;
                 };
                 int issued = 0;
+                // tile n's coordinates are looked up while the loop waits for its stage
+                // (a paged cache's block-table entry is a load of its own)
+                int y = 0, z = 0;
+                bool page_ok = ntiles > 0 && coords(0, y, z);
                 for (int n = 0; n < ntiles; ++n) {
                     const int s = n % kRing;
                     // Without a preceding grid, every CTA starts at once: the first tile
@@ -445,8 +449,6 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         raise_abort<kSplit>(sm, p, peer);
                         break;
                     }
-                    int y, z;
-                    const bool page_ok = coords(n, y, z);
                     if (!page_ok) {
                         set_status(p.status, MLA_ERR_PAGE);
                         y = p.num_pages * p.page_size;  // wholly out of range: the box reads as zeros
@@ -471,6 +473,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
                         }
                     }
                     issued = n + 1;
+                    if (n + 1 < ntiles) page_ok = coords(n + 1, y, z);
                 }
                 // every issued copy must land before this CTA may exit
                 const int first = issued > kRing ? issued - kRing : 0;
@@ -799,6 +802,8 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
         bool ok = true;
         int last_bar = -1;       // last tile whose pair barrier this thread passed
         float sc[kHalf];  // this CTA's (split: partial) scores of the current tile
+        // paged: the block-table entry of the current tile, loaded one tile ahead
+        int page_cur = (kPaged && !kSparse && ntiles > 0) ? __ldg(p.block_table + (long long)b * p.max_pages + t0 / p.page_size) : 0;
         if (ntiles > 0) {
             float s0[kHalf];
             if (!warp_wait(sm, &sm.s_full, 0)) raise_abort<kSplit>(sm, p, peer);
@@ -811,6 +816,9 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             for (int j = 0; j < kHalf; ++j) sc[j] = s0[j];
         }
         for (int n = 0; n < ntiles; ++n) {
+            const int page_n = page_cur;
+            if (kPaged && !kSparse && n + 1 < ntiles)
+                page_cur = __ldg(p.block_table + (long long)b * p.max_pages + (t0 + (n + 1) * kTile) / p.page_size);
             // next tile's scores (the MMA computes S(n+1) as soon as S(n) was read)
             float sn[kHalf];
             const bool more = n + 1 < ntiles;
@@ -851,10 +859,7 @@ __global__ void __launch_bounds__(threads_of(kSparse, kFp8), 1)
             // mask (only tiles that reach past a limit) and half-row maximum
             const int tok0 = t0 + n * kTile;
             bool tile_ok = true;
-            if (kPaged && !kSparse) {
-                const int page = __ldg(p.block_table + (long long)b * p.max_pages + tok0 / p.page_size);
-                tile_ok = page >= 0 && page < p.num_pages;  // tokens of a bad page are skipped
-            }
+            if (kPaged && !kSparse) tile_ok = page_n >= 0 && page_n < p.num_pages;  // tokens of a bad page are skipped
             // sparse: the producer's per-row flags (listed, visible to this block's query, good page)
             const unsigned long long vmask = kSparse ? sm.valid[n % kRing] : 0ull;
             const bool whole = kSparse ? vmask == ~0ull
