@@ -326,7 +326,8 @@ class DecodeRun:
                                max_seq_len=int(inp["seq_lens"].max()), num_splits=args.splits, kv_scale=self.kv_scale)
         self.splits = mla.decode_num_splits(prob, self.dec.cache) if args.splits == 0 else args.splits
         self.balanced = plan_is_balanced(prob, self.dec.cache, args.splits)
-        self.plan = (f"balanced ({self.splits} tile ranges per 128-row block)" if self.balanced
+        self.plan = ((f"balanced ({self.splits} tile ranges per 128-row block)" if self.splits > 0
+                      else "balanced (asked for)") if self.balanced
                      else f"split plan ({self.splits} pieces a split sequence)" if self.splits > 1 else "unsplit")
         self.dev = dev
         self.eager_step = lambda: self.dec.step(d["q_nope"], d["q_rope"])

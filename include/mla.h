@@ -186,9 +186,9 @@ MLA_API int mla_decode_num_splits(const mla_dims *dims, const mla_cache *cache);
  * lse fp32 [B][s_q][H].  num_splits 0 = the library's choice, else 1..64: every
  * sequence in num_splits pieces; MLA_SPLITS_BALANCED the balanced plan (see
  * there).  The library's choice splits every sequence while the pieces fit one
- * wave of the GPU, or, with CTA pairs and a bf16 cache, takes the balanced plan
- * when, with every sequence at max_seq_len, it gives a pair at least 16 tiles
- * fewer than the split plan; with more 128-row work items than a
+ * wave of the GPU, or, with CTA pairs and a contiguous bf16 cache, takes the
+ * balanced plan when, with every sequence at max_seq_len, it gives the busiest
+ * pair at least 16 tiles fewer than the split plans below; with more 128-row work items than a
  * wave holds, it leaves them whole except those of a last, partly filled wave,
  * whose sequences (the last ones of the batch) are split to fill that wave; their
  * pieces are the last work items of the same grid.  With a bf16 cache, up to

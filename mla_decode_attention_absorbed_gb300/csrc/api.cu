@@ -188,12 +188,13 @@ DecodePlan balanced_plan(const mla_dims *d, const mla_cache *c) {
 
 // The library's plan (requested == 0), else `requested` pieces for every
 // sequence (MLA_SPLITS_BALANCED: the balanced plan, which the caller checked is
-// supported).  In one wave of work items, the history is split to fill the wave;
-// with CTA pairs and a bf16 cache the balanced plan replaces that split when, with
-// every sequence at max_seq_len, it gives a pair at least kBalancedMinGain tiles
-// fewer (the balanced kernel's own costs, a later first score and the in-launch
-// merge, come to about that many tiles; measured: 128 -> 108 tiles a pair wins,
-// 64 -> 54 loses).  When the work items fill more than one wave of clusters and
+// supported).  In one wave of work items, the history is split to fill the wave.
+// With CTA pairs and a bf16 cache the balanced plan replaces the split plans when,
+// with every sequence at max_seq_len, it gives the busiest pair slot at least
+// kBalancedMinGain tiles fewer (the balanced kernel's own costs, a later first
+// score, the hand-overs and the in-launch merge, come to about that many tiles;
+// measured: 128 -> 108 tiles a pair wins 8 %, 64 -> 54 loses 6 %, spec's 448 ->
+// 432 wins 3 %), on a contiguous cache.  When the work items fill more than one wave of clusters and
 // the last wave is only partly used, the sequences of that last wave are split
 // over the whole of it instead: the ones before run unsplit and write their rows
 // directly, and only the tail's pieces are merged.  The wave arithmetic assumes
@@ -203,8 +204,9 @@ DecodePlan balanced_plan(const mla_dims *d, const mla_cache *c) {
 // which only the device knows; up to 1024 sequences, bf16 caches), so that a long
 // sequence does not start in the last wave; with equal lengths the order is the
 // batch order.
-DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
-    if (requested == MLA_SPLITS_BALANCED) return balanced_plan(d, c);
+// The split plans alone (requested > 0: that many pieces; 0: the choice above
+// without the balanced plan).
+DecodePlan split_plan(const mla_dims *d, const mla_cache *c, int requested) {
     const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
     const long long tiles = (maxL + 63) / 64;
     const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
@@ -213,17 +215,8 @@ DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
     DecodePlan pl{plan_splits_len(d, maxL, requested), 0, 1, false, 0};
     pl.lpt = pl.splits == 1 && units > slots && d->B <= kMaxOrdered && c->kv_dtype == MLA_KV_BF16;
     if (requested > 0) return pl;
-    if (units <= slots) {
-        if (units > 0 && balanced_supported(d, c)) {
-            const DecodePlan bp = balanced_plan(d, c);
-            const long long per_split = (tiles + pl.splits - 1) / pl.splits;
-            const long long per_balanced = (d->B * tiles + bp.persist_groups - 1) / bp.persist_groups;
-            if (per_split - per_balanced >= kBalancedMinGain) return bp;
-        }
-        return pl;
-    }
     const long long rem = units % slots;
-    if (pl.splits > 1 || rem == 0) return pl;
+    if (units <= slots || pl.splits > 1 || rem == 0) return pl;
     const long long b_tail = (rem + row_blocks - 1) / row_blocks;
     if (b_tail >= d->B) return pl;
     long long k = slots / (b_tail * row_blocks);
@@ -234,6 +227,31 @@ DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
     pl.b_tail = (int)b_tail;
     pl.tail_splits = (int)k;
     return pl;
+}
+
+DecodePlan plan_decode(const mla_dims *d, const mla_cache *c, int requested) {
+    if (requested == MLA_SPLITS_BALANCED) return balanced_plan(d, c);
+    const DecodePlan pl = split_plan(d, c, requested);
+    const long long row_blocks = ((long long)d->s_q * d->H + 127) / 128;
+    const long long units = (long long)d->B * row_blocks;
+    const long long slots = d->d_c > 256 ? num_sms() / 2 : num_sms();
+    // only with a contiguous cache: on a paged one the balanced kernel measured
+    // slower at equal tiles (ragged paged 766 against 700 us, dsv3 paged 118.7
+    // against 111.1 contiguous)
+    if (requested != 0 || units == 0 || c->block_table != nullptr || !balanced_supported(d, c)) return pl;
+    const long long maxL = c->max_seq_len > 0 ? c->max_seq_len : cache_capacity(c);
+    const long long tiles = (maxL + 63) / 64;
+    // tiles the busiest slot streams, every sequence at max_seq_len
+    long long per_split;
+    if (units <= slots) {
+        per_split = (tiles + pl.splits - 1) / pl.splits;
+    } else {
+        per_split = (units / slots) * tiles;
+        if (units % slots) per_split += pl.b_tail ? (tiles + pl.tail_splits - 1) / pl.tail_splits : tiles;
+    }
+    const DecodePlan bp = balanced_plan(d, c);
+    const long long per_balanced = (d->B * tiles + bp.persist_groups - 1) / bp.persist_groups;
+    return per_split - per_balanced >= kBalancedMinGain ? bp : pl;
 }
 
 // Bytes of the work order (sequence of each work-order position) after the status word.

@@ -143,9 +143,9 @@ def test_balanced_plan_for_pair_kernels(lib):
     dealt out to groups of pairs, one group per 76 // (128-row blocks) pair slots,
     capped so that a range holds at least 8 tiles of what max_seq_len allows; the
     workspace holds the merge counters, the tile prefix, the (m, l) hand-over and
-    two bf16 pieces per pair.  The library's choice takes it only in one wave of
-    work items and where it gives a pair at least 16 tiles fewer than the split
-    plan; FP8 caches, one-CTA widths and 4096 sequences or more cannot have it."""
+    two bf16 pieces per pair.  The library's choice takes it on a contiguous cache
+    where it gives the busiest pair slot at least 16 tiles fewer than the split
+    plans; FP8 caches, one-CTA widths and 4096 sequences or more cannot have it."""
     def rup(n):
         return (n + 255) // 256 * 256
 
@@ -175,13 +175,25 @@ def test_balanced_plan_for_pair_kernels(lib):
     assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c32), 0) == balanced_bytes(16, 76, 1)
     # 16 x 4096 tokens: 16 tiles a piece against 14: the split plan
     assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c)) == 4
-    # more work items than a wave of 76 pairs: the tail plan (256 items = 3 waves + 28)
+    # more than one wave of 76 pairs (256 items = 3 waves + 28): the busiest slot
+    # streams 3 x 128 + 64 tiles on the tail plan, 432 balanced (19 ranges a block):
+    # the balanced plan on a contiguous cache, the tail plan on a paged one
     d = dsv3(B=64, s_q=4).dims()
     c8 = fake_cache(8192)
-    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c8)) == 2  # 76 // 28
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c8)) == 19
+    assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c8), 0) == balanced_bytes(64, 76, 4)
+    c8p = fake_cache(8192, True)
+    assert lib.mla_decode_num_splits(ctypes.byref(d), ctypes.byref(c8p)) == 2  # 76 // 28
     tail_rows = 7 * 2 * 4 * 128  # the last 7 sequences, 2 pieces, 512 rows each
-    need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c8), 0)
+    need = lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c8p), 0)
     assert tail_rows * 512 * 4 <= need < 2 * tail_rows * 512 * 4
+    # one wave on a paged cache keeps the split plan even where the tiles favour the
+    # balanced one (16 x 32768 tokens: 4 pieces)
+    d16 = dsv3(B=16, s_q=1).dims()
+    assert lib.mla_decode_num_splits(ctypes.byref(d16), ctypes.byref(fake_cache(32768, True))) == 4
+    # many sequences: 1000 x 4096 tokens, 843 tiles the busiest slot either way: the tail plan
+    d1k = dsv3(B=1000, s_q=1).dims()
+    assert lib.mla_decode_num_splits(ctypes.byref(d1k), ctypes.byref(c)) == 6
     # an explicit count keeps the split plan
     d = dsv3(B=64, s_q=1).dims()
     assert lib.mla_decode_workspace_size(ctypes.byref(d), ctypes.byref(c), 2) >= 64 * 2 * 128 * 512 * 4
