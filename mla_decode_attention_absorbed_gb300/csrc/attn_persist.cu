@@ -50,7 +50,7 @@ constexpr uint32_t kBarEpi = 6;    // named barrier of the epilogue warps (128 t
 constexpr uint32_t kBarMerge = 7;  // named barrier of the whole block, for the merges at the end
 constexpr int kMergeBatch = 4;       // pieces whose (m, l) one thread loads at once
 constexpr int kMergeRowsStep = 64;   // rows of a merge block (one piece's half of the 128)
-constexpr uint64_t kMergeWaitNs = 1000000000ull;  // bound of a merge step's wait for its copies
+constexpr uint64_t kMergeWaitNs = 1000000000ull;  // bound of a merge wave's wait for its copies
 static_assert(kPThreads / 32 * 4 == kMergeRowsStep, "a merge step gives each warp 4 rows");
 // Register split of the 512-thread launch (128 a thread): the softmax warpgroups
 // take 152, the role and epilogue warpgroups 104 (2 x 128 x 152 + 2 x 128 x 104 =
@@ -70,7 +70,7 @@ struct PWalk {
     long long S;  // its first tile
 };
 
-// Bounded wait for a merge step's copies (global to this CTA's shared memory,
+// Bounded wait for a merge wave's copies (global to this CTA's shared memory,
 // so they end by themselves; the bound does not give up on an abort, as no copy
 // may still be landing when the CTA exits).
 __device__ __forceinline__ void merge_wait(Smem &sm, const AttnParams &p, uint32_t parity) {

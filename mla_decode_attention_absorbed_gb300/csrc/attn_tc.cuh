@@ -93,7 +93,7 @@ struct Smem {
     uint64_t o_last;       // the item's last P . V completed
     uint64_t o_free;       // the epilogue warps drained the item's O
     uint64_t ml_ready[2];  // by item parity: the softmax warps left the item's (m, l)
-    uint64_t merge_full;   // the pieces' rows a merge step needs landed in the ring
+    uint64_t merge_full;   // a merge wave's rows and (m, l) landed in the ring
     int walk_b;            // the sequence holding the first tile of this pair's range
     int n_pending;         // merges this CTA owes (it wrote the sequence's last piece): at most 2
     int pend_b[2];         // their sequences
