@@ -48,7 +48,7 @@ constexpr int kPThreads = 512;  // softmax 0-7, producer 8, score MMAs 9, exchan
 constexpr int kEpiWarp0 = 12;
 constexpr uint32_t kBarEpi = 6;    // named barrier of the epilogue warps (128 threads)
 constexpr uint32_t kBarMerge = 7;  // named barrier of the whole block, for the merges at the end
-constexpr int kMergeBatch = 4;       // pieces whose (m, l) one thread loads at once
+constexpr int kMergeBatch = 8;       // pieces whose (m, l) one thread loads at once
 constexpr int kMergeRowsStep = 64;   // rows of a merge block (one piece's half of the 128)
 constexpr uint64_t kMergeWaitNs = 1000000000ull;  // bound of a merge wave's wait for its copies
 static_assert(kPThreads / 32 * 4 == kMergeRowsStep, "a merge step gives each warp 4 rows");
@@ -69,6 +69,16 @@ struct PWalk {
     int b;        // next sequence to look at
     long long S;  // its first tile
 };
+
+// The pieces' rows in the workspace: for each (pair, slot) 128 rows of d_c
+// columns, stored as the first CTA's 128 x 256 block (its columns [0, 256)) and
+// then the second CTA's 128 x (d_c - 256), so that a CTA's rows of a piece are
+// contiguous (a merge fetches 64 of them with one bulk copy).  row0: the piece's
+// first row ((pair * 2 + slot) * 128); row r of the CTA's block at + r * g.vn.
+template <class T>
+__device__ __forceinline__ T *piece_rows(T *part16, long long row0, int d_c, uint32_t rank) {
+    return part16 + row0 * d_c + (long long)rank * kRows * 256;
+}
 
 // Bounded wait for a merge wave's copies (global to this CTA's shared memory,
 // so they end by themselves; the bound does not give up on an abort, as no copy
@@ -133,17 +143,17 @@ __device__ __forceinline__ void merge_pending(Smem &sm, const AttnParams &p, con
                 mbar_arrive_expect_tx(&sm.merge_full, bytes);
             }
             named_bar(kBarMerge, kPThreads);  // the ring and the (m, l) buffer are free again
-            if (threadIdx.x < nb * kMergeRowsStep) {
-                const int slot = threadIdx.x / kMergeRowsStep, rr = threadIdx.x % kMergeRowsStep;
+            if (threadIdx.x < nb) {  // one thread a block: its rows are contiguous, one copy each
+                const int slot = threadIdx.x;
                 const int bi = w0 + slot, h = (bi / np) * kMergeRowsStep, j = bi % np;
                 const int rows_here = max(0, min(kMergeRowsStep, rows_total - (rb * kRows + h)));
-                const long long pr0 = piece_row(j) + h;
-                if (rr < rows_here)
-                    bulk_load(stage + (size_t)(slot * kMergeRowsStep + rr) * row_bytes, part16 + (pr0 + rr) * p.d_c + g.k0,
-                              row_bytes, &sm.merge_full);
-                if (rr == 0 && rows_here > 0)
-                    bulk_load(blk_ml + slot * kMergeRowsStep, p.part_ml + pr0 * 4, (uint32_t)rows_here * sizeof(float4),
+                const long long pr0 = piece_row(j);
+                if (rows_here > 0) {
+                    bulk_load(stage + (size_t)slot * kMergeRowsStep * row_bytes, piece_rows(part16, pr0, p.d_c, rank) + (long long)h * g.vn,
+                              (uint32_t)rows_here * row_bytes, &sm.merge_full);
+                    bulk_load(blk_ml + slot * kMergeRowsStep, p.part_ml + (pr0 + h) * 4, (uint32_t)rows_here * sizeof(float4),
                               &sm.merge_full);
+                }
             }
             if (w0 == 0 && threadIdx.x < kRows) {  // under the first wave's copies
                 const int r = threadIdx.x;
@@ -663,7 +673,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const bool any = l_row > 0.f;
                 const float inv = any ? 1.f / l_row : 0.f;
                 __nv_bfloat16 *dst = it.out < 0 ? p.o_lat + row_index(it.b, gr) * p.d_c + g.k0
-                                                : part16 + prow * p.d_c + g.k0;
+                                                : piece_rows(part16, prow - r, p.d_c, rank) + (long long)r * g.vn;
                 for (int c = 0; c < g.vn; c += 32) {
                     uint32_t u[2][16];
 #pragma unroll
