@@ -57,6 +57,16 @@ CASES = [
                                     len_hi=300, paged=True, seed=22), 2),
     ("pair_dc448_rope32", MLAConfig("q3", B=2, H=128, d_c=448, d_rope=32, d_nope=128, d_v=128, s_q=3, len_lo=3,
                                     len_hi=260, seed=23), 0),
+    # the balanced plan on the same shapes: its pieces are stored per CTA (the second CTA's
+    # block d_c - 256 columns wide), two query tokens share a row block, three row blocks
+    ("contig_sq4_balanced", MLAConfig("c4", B=2, s_q=4, len_lo=4, len_hi=300, seed=4, **DSV3_DIMS),
+     mla.SPLITS_BALANCED),
+    ("pair_dc384_rope48_balanced", MLAConfig("q1", B=2, H=64, d_c=384, d_rope=48, d_nope=64, d_v=64, s_q=2,
+                                             len_lo=70, len_hi=400, seed=21), mla.SPLITS_BALANCED),
+    ("pair_dc320_rope16_balanced", MLAConfig("q2", B=3, H=128, d_c=320, d_rope=16, d_nope=64, d_v=64, s_q=1,
+                                             len_lo=1, len_hi=300, paged=True, seed=22), mla.SPLITS_BALANCED),
+    ("pair_dc448_rope32_balanced", MLAConfig("q3", B=2, H=128, d_c=448, d_rope=32, d_nope=128, d_v=128, s_q=3,
+                                             len_lo=3, len_hi=260, seed=23), mla.SPLITS_BALANCED),
 ]
 
 
